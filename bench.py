@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Benchmark: GEMM TFLOP/s (2MNK / t) of C = A x B, row-major, on GB300.
+
+One step is one call of the library's C entry point on one batch of
+synthetic input resident in HBM (dispatch, optional re-pitch, the GEMM
+kernel with its loads, MMAs and epilogue).  The headline line times the
+TF32 tensor-core path at M = N = K = 8192; the same run also times every
+other mode (FP32 SIMT and 3xTF32 at 8192^3, BF16 and TF32 at the
+16384 x 14336 x 4096 transformer-layer shape) and reports them under
+"modes".  Inputs are larger than L2 (129 MB), so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode tf32|3xtf32|simt|bf16]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Multi-GPU (launched by torch.distributed.run): every rank runs its own
+replica (GEMM has no exchange step here); value = all ranks' flops / the
+slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/t) at 8192³ per mode; % of FP32/TF32/BF16 dense peak"
+UNIT = "TFLOP/s"
+# Nominal dense tensor rates (PFLOP/s): the ratio converts the measured BF16
+# peak into peaks for the other tensor-core types.
+NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+
+# ---------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--mode", choices=["tf32", "3xtf32", "simt", "bf16"], default="tf32")
+    p.add_argument("--no-modes", action="store_true", help="headline only, skip the per-mode table")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if a.steps < 1:
+        p.error("--steps must be >= 1")
+    return a
+
+
+def workload_for(mode, transformer=False):
+    from dense_gemm_f32_gb300 import inputs
+
+    if mode == "bf16":
+        return inputs.TRANSFORMER_BF16
+    return inputs.TRANSFORMER_F32 if transformer else inputs.SQUARE_8192
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    except (OSError, ValueError, KeyError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def mode_peak(mode, peaks, num_sms):
+    """(bound, peak TFLOP/s, how) for a mode's kernel timed in a short loop."""
+    if mode == "simt":
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        return "alu", num_sms * 128 * 2 * mhz * 1e6 / 1e12, (
+            f"{num_sms} SMs x 128 FP32 lanes x 2 flop x {mhz:.0f} MHz")
+    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    if mode == "bf16":
+        return "tensor", bf16, "measured cuBLAS bf16 burst"
+    r = NOMINAL_PF["tf32"] / NOMINAL_PF["bf16"]
+    return "tensor", bf16 * r, f"measured bf16 burst x nominal tf32/bf16 ratio {r:.4f}"
+
+
+def source_sha(mode):
+    csrc = os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc")
+    files = ["simt.cu"] if mode == "simt" else ["tc.cu", "ptx.cuh"]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(mode, workload_name):
+    """DRAM bytes per launch from profiles/dram_traffic.md, or None when the
+    kernel's source has changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha(mode)
+    with open(path, encoding="utf-8") as f:
+        for ln in f:
+            cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == mode and cells[1] == workload_name:
+                if cells[2] != sha:
+                    return None
+                try:
+                    return float(cells[3])
+                except ValueError:
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+        return self
+
+    def stop(self):
+        rows = []
+        if self.proc is None:
+            return rows
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        for ln in self.file:
+            c = [x.strip() for x in ln.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(c[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + c[0].split(".")[1]) if "." in c[0] else 0.0
+                rows.append({"t": ts + frac, "sm": float(c[1]), "max": float(c[2]),
+                             "reasons": {"hw_slowdown": c[5], "hw_thermal_slowdown": c[6],
+                                         "sw_thermal_slowdown": c[7], "sw_power_cap": c[8]}})
+            except ValueError:
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+
+def summarize_clocks(rows, windows):
+    """Median SM clock and active throttle reasons over samples inside any of
+    the timed windows (wall-clock (start, end) pairs)."""
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                "note": "nvidia-smi unavailable"}
+    inside = [r for r in rows if any(a - 0.05 <= r["t"] <= b + 0.05 for a, b in windows)]
+    note = "samples inside the timed regions"
+    if not inside:
+        lo = min(a for a, _ in windows) - 1.0
+        hi = max(b for _, b in windows) + 1.0
+        inside = [r for r in rows if lo <= r["t"] <= hi]
+        note = "no sample fell inside a timed region; samples within 1 s of them"
+    if not inside:
+        inside, note = rows, "all samples of the run"
+    reasons = sorted({k for r in inside for k, v in r["reasons"].items()
+                      if v.lower() in ("active", "1", "yes")})
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+            "sm_max_mhz": max(r["max"] for r in inside), "reasons": reasons,
+            "samples": len(inside), "note": note}
+
+
+def aggregate(local_ms, world, flops_per_rank, steps, all_max):
+    """Whole-job numbers from this rank's timed milliseconds: all ranks'
+    flops over the slowest rank's time (`all_max` reduces a float by max)."""
+    t_ms = all_max(local_ms)
+    total = world * flops_per_rank * steps
+    return {"ms_total": t_ms, "ms_per_step": t_ms / steps, "value": total / (t_ms * 1e-3) / 1e12}
+
+
+# ------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x, device=None):
+        if not self.pg:
+            return x
+        import torch
+
+        t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------- CPU arm
+def cpu_oracle_rate(seconds, chunk=8):
+    """The oracle as it stands, on the host cores, over the first rows of the
+    8192^3 workload until `seconds` have passed.  (TFLOP/s, rows, threads, s)"""
+    import numpy as np
+
+    import oracle
+    from dense_gemm_f32_gb300 import inputs
+
+    w = inputs.SQUARE_8192
+    A, B = inputs.make(w)
+    An, Bn = A.numpy(), B.numpy()
+    threads = oracle.max_threads()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        rows = np.arange(done, done + chunk) % w.M
+        oracle.gemm_rows(An, Bn, rows, with_abs=False)
+        done += chunk
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    flops = 2.0 * done * w.N * w.K
+    return flops / el / 1e12, done, threads, el
+
+
+def run_reference(args, dist):
+    """--impl reference: the CPU oracle timed as the reference arm."""
+    if dist.rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from dense_gemm_f32_gb300 import inputs
+
+    w = inputs.SQUARE_8192
+    A, B = inputs.make(w)
+    An, Bn = A.numpy(), B.numpy()
+    rows_per_step = 16
+    threads = oracle.max_threads()
+    nxt = 0
+
+    def step():
+        nonlocal nxt
+        rows = (np.arange(rows_per_step) + nxt) % w.M
+        nxt += rows_per_step
+        oracle.gemm_rows(An, Bn, rows, with_abs=False)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    value = flops / el / 1e12
+    sample = (f"{rows_per_step} full rows of C (all {w.N} columns, K={w.K}) per step of the "
+              f"{w.name} workload, FP64 accumulation")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded uniform[-1,1))",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "mode": "cpu-oracle"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def device_inputs(w, mode, device):
+    import torch
+
+    from dense_gemm_f32_gb300 import inputs
+
+    A, B = inputs.make(w)
+    if mode == "bf16" and not w.bf16:
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    return A, B, A.to(device), B.to(device)
+
+
+def time_device(mode, Ad, Bd, C, steps, warmup, dist, device):
+    """Device time of `steps` back-to-back calls (inputs resident in HBM)."""
+    import torch
+
+    import dense_gemm_f32_gb300 as dg
+
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        dg.matmul(Ad, Bd, mode=mode, out=C)
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    n0 = dg.dgemm_kernel_launches()
+    w0 = time.time()
+    for i in range(steps):
+        ev[i].record(stream)
+        dg.matmul(Ad, Bd, mode=mode, out=C)
+    ev[steps].record(stream)
+    torch.cuda.synchronize(device)
+    w1 = time.time()
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    launches = dg.dgemm_kernel_launches() - n0
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total = ev[0].elapsed_time(ev[steps])
+    return {"ms_total": total, "per_step_ms": per, "launches": launches, "window": (w0, w1)}
+
+
+def time_e2e(mode, A, B, steps, warmup, dist, device):
+    """Same metric through the public API with host buffers: each step copies
+    A and B from pinned host memory, runs the GEMM and reads C back."""
+    import torch
+
+    import dense_gemm_f32_gb300 as dg
+
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    M, N = A.shape[0], B.shape[1]
+    Ch = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    Ad = torch.empty_like(Ah, device=device)
+    Bd = torch.empty_like(Bh, device=device)
+    Cd = torch.empty((M, N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        dg.matmul(Ad, Bd, mode=mode, out=Cd)
+        Ch.copy_(Cd, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    h2d = Ah.numel() * Ah.element_size() + Bh.numel() * Bh.element_size()
+    d2h = Ch.numel() * Ch.element_size()
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+def run_ours(args, dist):
+    import torch
+
+    import dense_gemm_f32_gb300 as dg
+    from dense_gemm_f32_gb300 import build
+
+    build.build()
+    dg.load()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    dist.init("nccl" if dist.world > 1 else "gloo")
+    props = torch.cuda.get_device_properties(device)
+    num_sms = props.multi_processor_count
+    peaks, peak_src = load_peaks()
+    sampler = ClockSampler(dist.local_rank).start()
+
+    # ---- headline
+    mode = args.mode
+    w = workload_for(mode)
+    A, B, Ad, Bd = device_inputs(w, mode, device)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
+    r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device)
+    agg = aggregate(r["ms_total"], dist.world, w.flops, args.steps, lambda x: dist.max(x, device))
+    windows = [r["window"]]
+    launches_per_step = r["launches"] / args.steps
+    mean_launch_ms = statistics.mean(r["per_step_ms"])
+    bound, peak, peak_how = mode_peak(mode, peaks, num_sms)
+    achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": profiled_traffic(mode, w.name),
+                "kernel": "tc_gemm_kernel" if mode != "simt" else "sgemm_simt_kernel",
+                "peak_source": f"{peak_src}: {peak_how}",
+                "per_launch_flops": w.flops, "launches_per_step": launches_per_step}
+
+    # ---- end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = time_e2e(mode, A, B, max(3, min(args.steps, 20)), 3, dist, device)
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e = aggregate(e2e_ms, dist.world, w.flops, e2e_steps, lambda x: dist.max(x, device))
+    del Ad, Bd, C
+    torch.cuda.empty_cache()
+
+    # ---- every other mode, same clocking
+    modes = {}
+    if not args.no_modes:
+        table = [("simt", False), ("tf32", False), ("3xtf32", False), ("bf16", True),
+                 ("tf32", True)]
+        for m, tr in table:
+            wm = workload_for(m, transformer=tr)
+            if m == mode and wm.name == w.name:
+                res = {"ms_per_step": statistics.median(r["per_step_ms"])}
+            else:
+                _, _, Adm, Bdm = device_inputs(wm, m, device)
+                Cm = torch.empty((wm.M, wm.N), dtype=torch.float32, device=device)
+                steps_m = max(5, min(args.steps, 20))
+                rm = time_device(m, Adm, Bdm, Cm, steps_m, 3, dist, device)
+                windows.append(rm["window"])
+                res = {"ms_per_step": statistics.median(rm["per_step_ms"])}
+                del Adm, Bdm, Cm
+                torch.cuda.empty_cache()
+            bm, pm, _ = mode_peak(m, peaks, num_sms)
+            tfl = wm.flops / (res["ms_per_step"] * 1e-3) / 1e12
+            modes[f"{m}@{wm.name}"] = {"tflops_median": round(tfl, 2), "bound": bm,
+                                       "peak": round(pm, 1), "frac": round(tfl / pm, 4),
+                                       "ms_median": round(res["ms_per_step"], 4)}
+    clocks = summarize_clocks(sampler.stop(), windows)
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if not args.no_cpu and dist.world == 1:
+        v, rows, threads, secs = cpu_oracle_rate(args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} full rows of C of the {inputs_name()} workload "
+                         f"({secs:.1f} s, FP64 accumulation, OpenMP over rows)"}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": agg["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"tf32": "tf32", "3xtf32": "3xtf32", "simt": "f32", "bf16": "bf16"}[mode],
+            "data": "synthetic (seeded, shapes and distributions of the workload)",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "mode": mode,
+                       "layout": "row-major, compact leading dimensions",
+                       "l2": "inputs larger than L2 (no flush needed)",
+                       "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": r["launches"],
+            "clocks": clocks,
+            "modes": modes,
+            "step_ms": {"median": statistics.median(r["per_step_ms"]),
+                        "min": min(r["per_step_ms"]), "max": max(r["per_step_ms"])},
+        }
+        print(json.dumps(line), flush=True)
+    st, where = dg.dgemm_watchdog_status(torch.cuda.current_stream(device).cuda_stream)
+    dist.close()
+    if st != dg.OK:
+        print(f"watchdog tripped at site {where:#x}", file=sys.stderr)
+        return 1
+    return 0
+
+
+def inputs_name():
+    from dense_gemm_f32_gb300 import inputs
+
+    return inputs.SQUARE_8192.name
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, dist)
+    return run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

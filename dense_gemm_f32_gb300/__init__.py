@@ -1,1 +1,86 @@
-"""GB300-native dense GEMM: C = A x B, row-major, on sm_103a."""
+"""GB300-native dense GEMM: C = A x B, row-major, on sm_103a.
+
+The library is the C ABI in include/dgemm.h (libdgemm.so, built from csrc/ by
+`build.py`).  This package binds it with ctypes under the same names
+(`gemm_f32_simt`, `gemm_f32_tc`, `gemm_bf16_tc`, ...: raw device pointers,
+status codes) and adds `matmul`, a convenience over torch CUDA tensors that
+only derives pointers, leading dimensions and the stream, allocates C, and
+raises on a non-zero status.  PyTorch is used for device memory and streams;
+all arithmetic runs in the library's kernels.  There is no fallback: without
+libdgemm.so every call raises.
+"""
+from ._lib import (  # noqa: F401  (re-exported C entry points)
+    ERR_ALIAS, ERR_ARCH, ERR_CUDA, ERR_INVALID_POINTER, ERR_INVALID_VALUE, ERR_MISALIGNED,
+    ERR_NULL_POINTER, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, LIB_PATH, OK, TC_3XTF32,
+    TC_TF32, LibraryMissing, dgemm_kernel_launches, dgemm_last_cuda_error, dgemm_status_string, dgemm_version,
+    dgemm_watchdog_status, gemm_bf16_tc, gemm_f32_simt, gemm_f32_tc, load,
+)
+
+MODES = ("simt", "tf32", "3xtf32", "bf16")
+
+
+class DgemmError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        msg = dgemm_status_string(status)
+        if status == ERR_CUDA:
+            msg += ": " + dgemm_last_cuda_error()
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def check(status, what=""):
+    if status != OK:
+        raise DgemmError(status, what)
+
+
+def _ld(X, cols):
+    """Leading dimension (elements) of a 2-D row-major tensor view."""
+    if X.dim() != 2:
+        raise ValueError("expected a 2-D matrix")
+    rows = X.shape[0]
+    if cols > 1 and X.stride(1) != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1)")
+    if rows <= 1:
+        return max(cols, 1)
+    return X.stride(0)
+
+
+def matmul(A, B, mode="tf32", out=None, stream=None):
+    """C = A @ B on the GPU through the C ABI.
+
+    A: (M, K), B: (K, N) CUDA tensors, float32 for modes simt / tf32 / 3xtf32,
+    bfloat16 for mode bf16; rows may be strided (leading dimension = stride(0)).
+    out: optional float32 (M, N) CUDA tensor view to overwrite.
+    stream: a torch.cuda.Stream or raw handle; default the current stream.
+    """
+    import torch
+
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {MODES}")
+    want = torch.bfloat16 if mode == "bf16" else torch.float32
+    if A.dtype != want or B.dtype != want:
+        raise TypeError(f"mode {mode} takes {want} inputs, got {A.dtype} and {B.dtype}")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (M, N):
+        raise ValueError("out must be a float32 (M, N) tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    lda, ldb, ldc = _ld(A, K), _ld(B, N), _ld(out, N)
+    pa, pb, pc = A.data_ptr(), B.data_ptr(), out.data_ptr()
+    if mode == "simt":
+        st = gemm_f32_simt(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    elif mode == "tf32":
+        st = gemm_f32_tc(TC_TF32, M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    elif mode == "3xtf32":
+        st = gemm_f32_tc(TC_3XTF32, M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    else:
+        st = gemm_bf16_tc(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    check(st, f"gemm ({mode})")
+    return out

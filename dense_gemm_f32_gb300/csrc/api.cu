@@ -1,0 +1,250 @@
+// api.cu -- the exported C ABI: argument validation, path choice, launch.
+//
+// Every check that can fail is done on the host before anything is
+// enqueued, so an invalid call never launches a kernel.  Order of checks:
+//   1. mode (gemm_f32_tc only)                      -> DGEMM_ERR_UNSUPPORTED
+//   2. sizes and leading dimensions                 -> DGEMM_ERR_INVALID_VALUE
+//   3. M == 0 or N == 0                             -> DGEMM_OK, nothing launched
+//   4. NULL pointers where there is work            -> DGEMM_ERR_NULL_POINTER
+//   5. pointer alignment to the element size        -> DGEMM_ERR_MISALIGNED
+//   6. C overlapping A or B                         -> DGEMM_ERR_ALIAS
+//   7. current device is compute capability 10.3    -> DGEMM_ERR_ARCH / DGEMM_ERR_CUDA
+//   8. A, B, C are device memory of this device     -> DGEMM_ERR_INVALID_POINTER
+// Steps 1-6 touch no CUDA API, so they behave the same on a machine without
+// a GPU.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/dgemm.h"
+#include "kernels.h"
+
+namespace dg {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace dg
+
+namespace {
+
+thread_local char g_cuda_err[512];
+
+int cuda_fail(cudaError_t e, const char *where) {
+  snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%s)", where, cudaGetErrorString(e),
+           cudaGetErrorName(e));
+  return DGEMM_ERR_CUDA;
+}
+
+// Per-device facts, looked up once.  state: 0 unknown, 1 supported, 2 not CC 10.3.
+struct DeviceInfo {
+  std::atomic<int> state{0};
+  int num_sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+
+int current_device(int *dev, int *num_sms) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (d < 0 || d >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device ordinal");
+  DeviceInfo &info = g_devices[d];
+  int st = info.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    info.num_sms = sms;
+    st = (major == 10 && minor == 3) ? 1 : 2;
+    info.state.store(st, std::memory_order_release);
+  }
+  if (st != 1) return DGEMM_ERR_ARCH;
+  *dev = d;
+  *num_sms = info.num_sms;
+  return DGEMM_OK;
+}
+
+// A, B and C must be memory that this device's kernels can address directly.
+int check_device_pointer(const void *p, int dev) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // the failed query's own, non-sticky error
+    return DGEMM_ERR_INVALID_POINTER;
+  }
+  if (at.type == cudaMemoryTypeManaged) return DGEMM_OK;
+  if (at.type == cudaMemoryTypeDevice && at.device == dev) return DGEMM_OK;
+  return DGEMM_ERR_INVALID_POINTER;
+}
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte range [lo, hi) spanned by a rows x cols row-major matrix.
+struct Span {
+  uintptr_t lo, hi;
+};
+inline Span span(const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t es) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  if (rows <= 0 || cols <= 0) return {lo, lo};
+  return {lo, lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * es)};
+}
+inline bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// Steps 2-8 of the check list.  *nothing_to_do is set when M or N is zero.
+int validate(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C,
+             int ldc, int in_bytes, bool *nothing_to_do, int *dev, int *num_sms) {
+  *nothing_to_do = false;
+  if (M < 0 || N < 0 || K < 0) return DGEMM_ERR_INVALID_VALUE;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return DGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) {
+    *nothing_to_do = true;
+    return DGEMM_OK;
+  }
+  if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return DGEMM_ERR_NULL_POINTER;
+  if (!aligned(C, 4)) return DGEMM_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(A, in_bytes) || !aligned(B, in_bytes))) return DGEMM_ERR_MISALIGNED;
+  if (K > 0) {
+    const Span c = span(C, M, N, ldc, 4);
+    if (overlap(c, span(A, M, K, lda, in_bytes)) || overlap(c, span(B, K, N, ldb, in_bytes)))
+      return DGEMM_ERR_ALIAS;
+  }
+  int st = current_device(dev, num_sms);
+  if (st != DGEMM_OK) return st;
+  if ((st = check_device_pointer(C, *dev)) != DGEMM_OK) return st;
+  if (K > 0) {
+    if ((st = check_device_pointer(A, *dev)) != DGEMM_OK) return st;
+    if ((st = check_device_pointer(B, *dev)) != DGEMM_OK) return st;
+  }
+  return DGEMM_OK;
+}
+
+int after_launch(cudaError_t e, const char *what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DGEMM_OK;
+}
+
+// TMA needs 16-byte aligned bases and row pitches that are multiples of 16 B.
+inline bool tma_ok(const void *p, int64_t ld, int es) { return aligned(p, 16) && (ld * es) % 16 == 0; }
+
+// Tensor-core GEMM with operands re-pitched into stream-ordered scratch when
+// their rows do not start on 16-byte boundaries.
+int run_tc(dg::TcKind kind, int M, int N, int K, const void *A, int lda, const void *B, int ldb,
+           float *C, int ldc, int num_sms, cudaStream_t stream) {
+  const int es = (kind == dg::TcKind::kBF16) ? 2 : 4;
+  const int64_t pitch_elems = 16 / es;
+  const void *Ause = A, *Buse = B;
+  int64_t lda_use = lda, ldb_use = ldb;
+  void *scratch = nullptr;
+  const bool a_ok = tma_ok(A, lda, es), b_ok = tma_ok(B, ldb, es);
+  cudaError_t e = cudaSuccess;
+  if (!a_ok || !b_ok) {
+    const int64_t lda2 = (K + pitch_elems - 1) / pitch_elems * pitch_elems;
+    const int64_t ldb2 = (N + pitch_elems - 1) / pitch_elems * pitch_elems;
+    const size_t a_bytes = a_ok ? 0 : (size_t)((int64_t)M * lda2 * es + 255) / 256 * 256;
+    const size_t b_bytes = b_ok ? 0 : (size_t)((int64_t)K * ldb2 * es + 255) / 256 * 256;
+    e = cudaMallocAsync(&scratch, a_bytes + b_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (re-pitch scratch)");
+    char *s = static_cast<char *>(scratch);
+    if (!a_ok) {
+      e = dg::launch_repitch(A, lda, s, lda2, M, K, es, num_sms, stream);
+      if (e != cudaSuccess) goto done;
+      Ause = s;
+      lda_use = lda2;
+    }
+    if (!b_ok) {
+      e = dg::launch_repitch(B, ldb, s + a_bytes, ldb2, K, N, es, num_sms, stream);
+      if (e != cudaSuccess) goto done;
+      Buse = s + a_bytes;
+      ldb_use = ldb2;
+    }
+  }
+  e = dg::launch_tc(kind, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
+done:
+  if (scratch != nullptr) {
+    cudaError_t e2 = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess && e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+  }
+  return after_launch(e, "tensor-core GEMM launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f32_simt(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                  float *C, int ldc, cudaStream_t stream) {
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  const bool ab_vec = aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0;
+  const bool c_vec = aligned(C, 16) && ldc % 4 == 0;
+  return after_launch(dg::launch_simt(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, stream),
+                      "SIMT GEMM launch");
+}
+
+int gemm_f32_tc(int mode, int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                float *C, int ldc, cudaStream_t stream) {
+  if (mode != DGEMM_TC_TF32 && mode != DGEMM_TC_3XTF32) return DGEMM_ERR_UNSUPPORTED;
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  return run_tc(mode == DGEMM_TC_TF32 ? dg::TcKind::kTF32 : dg::TcKind::k3xTF32, M, N, K, A, lda,
+                B, ldb, C, ldc, sms, stream);
+}
+
+int gemm_bf16_tc(int M, int N, int K, const unsigned short *A, int lda, const unsigned short *B,
+                 int ldb, float *C, int ldc, cudaStream_t stream) {
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 2, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  return run_tc(dg::TcKind::kBF16, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
+}
+
+const char *dgemm_status_string(int status) {
+  switch (status) {
+    case DGEMM_OK: return "success";
+    case DGEMM_ERR_INVALID_VALUE: return "invalid value: negative size or leading dimension too small";
+    case DGEMM_ERR_NULL_POINTER: return "null pointer for A, B or C";
+    case DGEMM_ERR_ALIAS: return "C overlaps A or B";
+    case DGEMM_ERR_UNSUPPORTED: return "unsupported mode";
+    case DGEMM_ERR_CUDA: return "CUDA error (see dgemm_last_cuda_error)";
+    case DGEMM_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103a)";
+    case DGEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case DGEMM_ERR_INVALID_POINTER: return "A, B or C is not device memory of the current device";
+    case DGEMM_ERR_WATCHDOG: return "a kernel gave up a bounded wait; its output is incomplete";
+    default: return "unknown status";
+  }
+}
+
+const char *dgemm_last_cuda_error(void) { return g_cuda_err; }
+
+int dgemm_watchdog_status(cudaStream_t stream, int *where) {
+  int code = 0;
+  cudaError_t e = dg::read_watchdog(stream, &code);
+  if (e != cudaSuccess) return cuda_fail(e, "watchdog read");
+  if (where) *where = code;
+  return code ? DGEMM_ERR_WATCHDOG : DGEMM_OK;
+}
+
+int dgemm_version(void) { return 100; }
+
+unsigned long long dgemm_kernel_launches(void) {
+  return dg::g_launches.load(std::memory_order_relaxed);
+}
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// kernels.h -- internal launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dg {
+
+// FP32 FFMA GEMM.  ab_vec: A and B rows start on 16-byte boundaries (base
+// pointers 16-byte aligned, lda % 4 == 0, ldb % 4 == 0).  c_vec: same for C.
+cudaError_t launch_simt(int M, int N, int K, const float *A, int64_t lda, const float *B,
+                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
+                        cudaStream_t stream);
+
+// C[i*ldc + j] = 0 for i < M, j < N (the empty sum, K == 0).
+cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
+                             cudaStream_t stream);
+
+// Element type of a tensor-core GEMM's operands.
+enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2 };
+
+// tcgen05 GEMM.  A (M x K) and B (K x N) row-major with leading dimensions in
+// elements; both must satisfy the TMA rules (16-byte aligned base, leading
+// dimension * element size a multiple of 16 bytes).  C fp32 row-major.
+cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
+                      int num_sms, cudaStream_t stream);
+
+// Copy a rows x cols matrix of elem_bytes-sized elements (4 or 2) from
+// (src, lds) to (dst, ldd); used to re-pitch operands whose rows do not start
+// on 16-byte boundaries.
+cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
+                           int cols, int elem_bytes, int num_sms, cudaStream_t stream);
+
+// Count one successful kernel launch (dgemm_kernel_launches).
+void count_launch();
+
+// Read and clear the device's watchdog word after synchronising `stream`.
+cudaError_t read_watchdog(cudaStream_t stream, int *code);
+
+}  // namespace dg

@@ -1,0 +1,526 @@
+// tc.cu -- dense GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// What it computes: C = A x B, row-major, C[i][j] = sum_k A[i][k] B[k][j]
+// ("第八课：GPU 如何完成矩阵乘法" section 一), by the tile decomposition
+// C_tile = sum_t A_tile,t x B_tile,t of section 九, with the tensor core doing
+// each tile's small matrix multiply-accumulate (section 二十一, "SGEMM 优化旅程"
+// Level 6) and the data supply decoupled from the math by an asynchronous,
+// multi-buffered copy pipeline (sections 二十三-二十五).
+//
+// Blackwell design (none of this is on the pages, which stop at WMMA):
+//  * Persistent kernel, one CTA per SM, walking 128 x BN output tiles in
+//    groups of kGroupM tile rows (L2 reuse of the A and B panels).
+//  * Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma (one
+//    thread) and owns the TMEM allocation, warps 2-5 drain the accumulator
+//    (tcgen05.ld -> registers -> global).  For 3xTF32, warps 6-9 split each
+//    staged fp32 tile into hi and lo TF32 parts in shared memory.
+//  * Operands: A (M x K, K contiguous) is K-major, B (K x N, N contiguous) is
+//    MN-major; both arrive by 2-D TMA boxes of one 128-byte swizzle row width
+//    into 128B-swizzled shared memory, which is the layout the MMA's shared
+//    memory descriptors describe.  TMA fills the out-of-range part of an edge
+//    box with zeros (the pages' zero-fill of partial tiles, section 二十六).
+//  * Accumulators: fp32 in tensor memory, two buffers of BN columns each, so
+//    the epilogue of tile i overlaps the main loop of tile i + 1.
+//  * Every wait is bounded (ptx.cuh); on a timeout the CTA records the site in
+//    the device watchdog word, drains what it issued, frees TMEM and returns.
+#include <cstdint>
+#include <cstdio>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dg {
+
+// Device watchdog word: 0, or the site code of the first wait that gave up.
+__device__ int g_watchdog = 0;
+
+namespace {
+
+constexpr int kGroupM = 8;
+constexpr int BM = 128;
+
+// Watchdog site codes (role * 16 + place).
+enum : int {
+  kSiteProducerEmpty = 0x11,
+  kSiteProducerDrain = 0x12,
+  kSiteMmaFull = 0x21,
+  kSiteMmaAccEmpty = 0x22,
+  kSiteMmaDrain = 0x23,
+  kSiteEpiAccFull = 0x31,
+  kSiteSplitFull = 0x41,
+};
+
+template <TcKind KIND, int BN_>
+struct Cfg {
+  static constexpr bool kBF16 = KIND == TcKind::kBF16;
+  static constexpr bool kSplit = KIND == TcKind::k3xTF32;
+  static constexpr int BN = BN_;
+  static constexpr int ES = kBF16 ? 2 : 4;        // operand element bytes
+  static constexpr int BK = 128 / ES;             // k per stage: one 128-B swizzle row
+  static constexpr int UMMA_K = 32 / ES;          // k per MMA instruction (32 bytes)
+  static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per stage (per product)
+  static constexpr int BOX_N = 128 / ES;          // N columns per B box
+  static constexpr int B_BOXES = BN / BOX_N;
+  static constexpr int A_BYTES = BM * 128;        // 128 rows x 128 B
+  static constexpr int B_BOX_BYTES = BK * 128;    // BK rows x 128 B
+  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int RAW_BYTES = A_BYTES + B_BYTES;               // what TMA writes
+  static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);  // + lo copies
+  static constexpr int STAGES = (kSplit ? 196608 : 196608) / STAGE_BYTES;
+  static constexpr int ACC_COLS = 2 * BN;                           // two fp32 accumulators
+  static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64
+                                   : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
+  static constexpr int kEpiWarp0 = 2, kEpiWarps = 4;
+  static constexpr int kSplitWarp0 = 6, kSplitWarps = kSplit ? 4 : 0;
+  static constexpr int THREADS = 32 * (2 + kEpiWarps + kSplitWarps);
+  // barriers: full[S], empty[S], split[S], acc_full[2], acc_empty[2], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
+
+  static_assert(BN % BOX_N == 0, "BN must be a whole number of B boxes");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  static_assert(STAGES >= 2, "pipeline needs at least two stages");
+  static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
+  static_assert(kSplitWarp0 == kEpiWarp0 + kEpiWarps, "split warps follow the epilogue warps");
+
+  // Instruction descriptor: D fp32, A/B TF32 or BF16, A K-major, B MN-major,
+  // N >> 3 at bit 17, M >> 4 at bit 24.
+  static constexpr uint32_t IDESC = (1u << 4) | ((kBF16 ? 1u : 2u) << 7) |
+                                    ((kBF16 ? 1u : 2u) << 10) | (0u << 15) | (1u << 16) |
+                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+};
+
+// Shared-memory matrix descriptor for a 128B-swizzled operand tile:
+// start address, leading / stride byte offsets (16-byte units), version 1,
+// base offset 0 (tiles are 1024-byte aligned), swizzle mode 2 = 128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm, int &tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int group = tile / per_group;
+  const int first = group * kGroupM;
+  const int gsize = min(tiles_m - first, kGroupM);
+  const int r = tile - group * per_group;
+  tm = first + r % gsize;
+  tn = r / gsize;
+}
+
+__device__ __forceinline__ void watchdog_trip(int site, volatile int *abort_flag) {
+  atomicCAS(&g_watchdog, 0, site);
+  *abort_flag = 1;
+}
+
+// Split x into hi + lo, both exactly representable in TF32: hi = x rounded to
+// TF32 (nearest, ties away), lo = x - hi (exact in fp32), lo rounded to TF32.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  uint32_t h, l;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+  const float r = x - __uint_as_float(h);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
+  hi = h;
+  lo = l;
+}
+
+template <TcKind KIND, int BN>
+__global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
+                   int N, int K, int64_t ldc, int c_vec) {
+  using G = Cfg<KIND, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzle atoms.
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+
+  const uint32_t bars = base + G::STAGES * G::STAGE_BYTES;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (G::STAGES + s); };
+  auto split_bar = [&](int s) { return bars + 8u * (2 * G::STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
+  uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::NUM_BARS * 8;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
+
+  auto a_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES); };
+  auto b_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES + G::A_BYTES); };
+  auto a_lo = [&](int s) { return a_tile(s) + (uint32_t)G::RAW_BYTES; };
+  auto b_lo = [&](int s) { return b_tile(s) + (uint32_t)G::RAW_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int kblocks = (K + G::BK - 1) / G::BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(split_bar(s), G::kSplitWarps > 0 ? G::kSplitWarps : 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), G::kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), G::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;  // stages loaded so far (for the drain on abort)
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, tiles_m, tiles_n, tm, tn);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+            if (!*abort_flag) watchdog_trip(kSiteProducerEmpty, abort_flag);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
+          tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, tm * BM);
+#pragma unroll
+          for (int j = 0; j < G::B_BOXES; ++j)
+            tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
+                        tn * BN + j * G::BOX_N, kb * G::BK);
+          ++issued;
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Wait (bounded) for the copies of the last stages issued, so that no
+        // TMA write lands after this CTA has left.
+        int s = stage;
+        uint32_t ph = phase;
+        const int n = issued < G::STAGES ? issued : G::STAGES;
+        for (int i = 0; i < n; ++i) {
+          if (--s < 0) {
+            s = G::STAGES - 1;
+            ph ^= 1u;
+          }
+          if (!mbar_wait(full_bar(s), ph)) atomicCAS(&g_watchdog, 0, kSiteProducerDrain);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
+          if (!*abort_flag) watchdog_trip(kSiteMmaAccEmpty, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const uint32_t ready = G::kSplit ? split_bar(stage) : full_bar(stage);
+          if (*abort_flag || !mbar_wait(ready, phase)) {
+            if (!*abort_flag) watchdog_trip(kSiteMmaFull, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < G::KSTEPS; ++k) {
+            // A: K-major, advance 32 bytes per MMA inside the swizzle row.
+            // B: MN-major, advance UMMA_K rows = UMMA_K / 8 atoms of 1024 B.
+            const uint32_t a_off = (uint32_t)(k * 32);
+            const uint32_t b_off = (uint32_t)(k * (G::UMMA_K / 8) * 1024);
+            const uint64_t ad = sw128_desc(a_tile(stage) + a_off, 16, 1024);
+            const uint64_t bd = sw128_desc(b_tile(stage) + b_off, G::B_BOX_BYTES, 1024);
+            const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+            if constexpr (G::kSplit) {
+              const uint64_t adl = sw128_desc(a_lo(stage) + a_off, 16, 1024);
+              const uint64_t bdl = sw128_desc(b_lo(stage) + b_off, G::B_BOX_BYTES, 1024);
+              umma_tf32(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
+              umma_tf32(d_tmem, ad, bdl, G::IDESC, 1u);      // A_hi B_lo
+              umma_tf32(d_tmem, ad, bd, G::IDESC, 1u);       // A_hi B_hi
+            } else if constexpr (G::kBF16) {
+              umma_f16(d_tmem, ad, bd, G::IDESC, accum);
+            } else {
+              umma_tf32(d_tmem, ad, bd, G::IDESC, accum);
+            }
+          }
+          umma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(acc));  // accumulator complete
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Drain: wait until every MMA issued above has completed before TMEM is
+      // released (on the normal path the epilogue has already seen them all).
+      umma_commit(drain_bar);
+      if (!mbar_wait(drain_bar, 0)) atomicCAS(&g_watchdog, 0, kSiteMmaDrain);
+    }
+  } else if (warp < G::kEpiWarp0 + G::kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int tm, tn;
+      tile_coords(tile, tiles_m, tiles_n, tm, tn);
+      // every lane waits, so that each one acquires the accumulator itself
+      bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
+      if (!ok && lane == 0 && !*abort_flag) watchdog_trip(kSiteEpiAccFull, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row = tm * BM + quarter * 32 + lane;
+      float *crow = C + (int64_t)row * ldc;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
+        tmem_wait_ld();
+        const int col = tn * BN + c0;
+        if (row < M) {
+          if (c_vec && col + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4 *>(crow + col + j) =
+                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col + j < N) crow[col + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  } else if constexpr (G::kSplit) {
+    // -------------------------------------------- 3xTF32 split (warps 6-9)
+    const int t = threadIdx.x - 32 * G::kSplitWarp0;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        // every lane waits: each acquires the TMA-written bytes it reads
+        bool got = !*abort_flag && mbar_wait(full_bar(stage), phase);
+        if (!got && lane == 0 && !*abort_flag) watchdog_trip(kSiteSplitFull, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        // The split is elementwise, so it is independent of the swizzle: the
+        // hi part overwrites the raw value, the lo part goes to the same
+        // offset of the lo copy.
+        uint4 *raw = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES);
+        uint4 *lo = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES + G::RAW_BYTES);
+        for (int i = t; i < G::RAW_BYTES / 16; i += 32 * G::kSplitWarps) {
+          const uint4 v = raw[i];
+          uint4 h, l;
+          split_tf32(__uint_as_float(v.x), h.x, l.x);
+          split_tf32(__uint_as_float(v.y), h.y, l.y);
+          split_tf32(__uint_as_float(v.z), h.z, l.z);
+          split_tf32(__uint_as_float(v.w), h.w, l.w);
+          raw[i] = h;
+          lo[i] = l;
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(split_bar(stage));
+        if (++stage == G::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();  // tcgen05.dealloc is .sync.aligned: the whole warp, converged
+    tc_fence_after();
+    tmem_dealloc(tmem_base, G::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D row-major tensor map: `rows` x `cols` elements, leading dimension `ld`,
+// box of box_cols x box_rows, 128-byte swizzle, zero fill out of range.
+bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es, int64_t rows,
+              int64_t cols, int64_t ld, int box_cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <TcKind KIND, int BN>
+cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
+                       int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
+                       cudaStream_t stream) {
+  using G = Cfg<KIND, BN>;
+  const CUtensorMapDataType dt =
+      G::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK)) return cudaErrorInvalidValue;
+  auto kern = tc_gemm_kernel<KIND, BN>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+__global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_bytes,
+                               uint8_t *__restrict__ dst, int64_t ldd_bytes, int rows,
+                               int64_t row_bytes, int64_t pad_bytes, int es) {
+  // one element per thread-iteration; the padding columns are zeroed
+  const int64_t per_row = (row_bytes + pad_bytes) / es;
+  const int64_t total = (int64_t)rows * per_row;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / per_row, c = (e - r * per_row) * es;
+    uint8_t *d = dst + r * ldd_bytes + c;
+    if (es == 4) {
+      *reinterpret_cast<uint32_t *>(d) =
+          c < row_bytes ? *reinterpret_cast<const uint32_t *>(src + r * lds_bytes + c) : 0u;
+    } else {
+      *reinterpret_cast<uint16_t *>(d) =
+          c < row_bytes ? *reinterpret_cast<const uint16_t *>(src + r * lds_bytes + c) : 0;
+    }
+  }
+}
+
+__global__ void read_watchdog_kernel(int *out) {
+  *out = g_watchdog;
+  g_watchdog = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
+                      int num_sms, cudaStream_t stream) {
+  switch (kind) {
+    case TcKind::kTF32:
+      return launch_cfg<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                            stream);
+    case TcKind::k3xTF32:
+      return launch_cfg<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                              stream);
+    case TcKind::kBF16:
+      return launch_cfg<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                            stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
+                           int cols, int elem_bytes, int num_sms, cudaStream_t stream) {
+  const int64_t total = (int64_t)rows * ldd;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+  if (blocks < 1) blocks = 1;
+  repitch_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const uint8_t *>(src), lds * elem_bytes, static_cast<uint8_t *>(dst),
+      ldd * elem_bytes, rows, (int64_t)cols * elem_bytes, (ldd - cols) * (int64_t)elem_bytes,
+      elem_bytes);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+cudaError_t read_watchdog(cudaStream_t stream, int *code) {
+  int *d = nullptr;
+  cudaError_t e = cudaMallocAsync(&d, sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  read_watchdog_kernel<<<1, 1, 0, stream>>>(d);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  int h = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  cudaError_t e2 = cudaFreeAsync(d, stream);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) *code = h;
+  return e;
+}
+
+}  // namespace dg

@@ -1,0 +1,167 @@
+/*
+ * dgemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Every entry point computes the plain row-major matrix product
+ *
+ *     C[i*ldc + j] = sum_{k=0}^{K-1} A[i*lda + k] * B[k*ldb + j],  0 <= i < M, 0 <= j < N
+ *
+ * as defined in "第八课：GPU 如何完成矩阵乘法" (Lesson 8: how a GPU does matrix
+ * multiplication), section 一 (C = A x B with A in R^{M x K}, B in R^{K x N},
+ * C_{i,j} = sum_k A_{i,k} B_{k,j}); the same formula opens "SGEMM 优化旅程",
+ * Level 1, and section 4.1 of "4. 矩阵乘法（GEMM）优化".  The pages use the
+ * compact row-major addressing A[row*K + k], B[k*N + col], C[row*N + col]
+ * (Lesson 8 section 四, section 二十八); these entry points take BLAS-style
+ * leading dimensions lda >= K, ldb >= N, ldc >= N, counted in elements.
+ *
+ * Semantics shared by all entry points
+ *   - C is OVERWRITTEN inside its M x N region (no alpha/beta: the pages store
+ *     the finished sum, C[row*N + col] = sum).  Elements of C outside that
+ *     region (the ldc - N gap at the end of each row) are never written.
+ *   - K == 0: the empty sum; the M x N region of C is set to zero.
+ *   - M == 0 or N == 0: nothing to do; DGEMM_OK with no launch (the pointers
+ *     are not looked at).
+ *   - Sizes are int, as in the pages' kernel signatures; all offsets are
+ *     computed in 64-bit.
+ *
+ * Pointers and ownership
+ *   - A, B and C are DEVICE pointers (cudaMalloc'd or managed memory) on the
+ *     current CUDA device, owned by the caller.  Host pointers are rejected
+ *     with DGEMM_ERR_INVALID_POINTER before anything is launched.
+ *   - Only natural element alignment is required (4 bytes for fp32, 2 for
+ *     bf16).  Any pointer or leading dimension, aligned to 16 bytes or not, is
+ *     accepted; the library chooses the load path itself.
+ *   - C must not overlap the bytes A or B span: DGEMM_ERR_ALIAS.
+ *
+ * Execution
+ *   - Asynchronous on `stream` (0 = the legacy default stream): the call
+ *     validates, enqueues and returns.  Work on the same stream is ordered.
+ *   - A launch failure, or a sticky error left by earlier work, is returned as
+ *     DGEMM_ERR_CUDA; dgemm_last_cuda_error() gives the CUDA message.
+ *   - Deterministic: the same inputs give bitwise identical C on every call
+ *     (no atomics, no split-K races).
+ *   - Thread-safe and re-entrant; the only mutable library state is a
+ *     per-thread error string and a per-device watchdog word (see
+ *     dgemm_watchdog_status).
+ *   - Some paths use temporary device memory, taken with cudaMallocAsync /
+ *     cudaFreeAsync on `stream` (stream-ordered, nothing kept between calls).
+ */
+#ifndef DGEMM_H
+#define DGEMM_H
+
+#include <cuda_runtime_api.h>   /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Every entry point returns one; only DGEMM_OK means the work
+ * was enqueued. */
+typedef enum {
+    DGEMM_OK = 0,
+    DGEMM_ERR_INVALID_VALUE = 1,   /* negative size, leading dimension too small */
+    DGEMM_ERR_NULL_POINTER = 2,    /* NULL A, B or C with work to do            */
+    DGEMM_ERR_ALIAS = 3,           /* C overlaps A or B                          */
+    DGEMM_ERR_UNSUPPORTED = 4,     /* unknown mode                               */
+    DGEMM_ERR_CUDA = 5,            /* CUDA runtime/driver error (see below)      */
+    DGEMM_ERR_ARCH = 6,            /* current device is not compute capability 10.3 */
+    DGEMM_ERR_MISALIGNED = 7,      /* pointer not aligned to its element size    */
+    DGEMM_ERR_INVALID_POINTER = 8, /* A, B or C is not device-accessible memory  */
+    DGEMM_ERR_WATCHDOG = 9         /* a kernel gave up a bounded wait (see dgemm_watchdog_status) */
+} dgemm_status_t;
+
+/* Tensor-core precision modes of gemm_f32_tc. */
+typedef enum {
+    DGEMM_TC_TF32 = 0,   /* operands read at TF32 precision (10-bit mantissa), FP32 accumulate */
+    DGEMM_TC_3XTF32 = 1  /* split precision: a = a_hi + a_lo, three TF32 products, FP32-grade result */
+} dgemm_tc_mode_t;
+
+/*
+ * gemm_f32_simt -- FP32 inputs, FP32 fused multiply-add on the CUDA cores.
+ *
+ * The register-blocked, shared-memory tiled form of the product: "SGEMM 优化旅程"
+ * Levels 2-5 (shared-memory tiles, padding against bank conflicts, double
+ * buffering, 8x8 register blocking per thread of a 128x128x8 block tile) and
+ * Lesson 8 sections 九-十九 (tile decomposition C_tile = sum_t A_tile,t B_tile,t,
+ * register accumulation, multi-level tiling, boundary zero-fill and masked
+ * stores of section 二十六).
+ * A: M x K fp32, row-major, leading dimension lda >= max(1, K).
+ * B: K x N fp32, row-major, leading dimension ldb >= max(1, N).
+ * C: M x N fp32, row-major, leading dimension ldc >= max(1, N); overwritten.
+ * Accuracy: |C - C_exact| <= 1e-5 * (|A| x |B|) elementwise; exact when every
+ * product and partial sum is an integer below 2^24.
+ */
+int gemm_f32_simt(int M, int N, int K,
+                  const float *A, int lda,
+                  const float *B, int ldb,
+                  float *C, int ldc,
+                  cudaStream_t stream);
+
+/*
+ * gemm_f32_tc -- FP32 inputs on the 5th-generation tensor cores (tcgen05).
+ *
+ * The tensor-core form of the product: "SGEMM 优化旅程" Level 6 and Lesson 8
+ * sections 二十一-二十三 (the tensor core computes a small D = A x B + C per
+ * instruction, and must be fed tiles through shared memory).  Operands are
+ * staged by TMA into swizzled shared memory, accumulated in tensor memory.
+ * mode = DGEMM_TC_TF32:   each operand is read at TF32 precision; accuracy
+ *                         |C - C_exact| <= 2e-3 * (|A| x |B|).
+ * mode = DGEMM_TC_3XTF32: each operand is split a = hi + lo (hi = a with the
+ *                         low 13 mantissa bits cleared, lo = a - hi, both
+ *                         exact TF32 values) and C = A_hi B_hi + A_hi B_lo +
+ *                         A_lo B_hi; accuracy <= 1e-5 * (|A| x |B|).
+ * Argument layout as gemm_f32_simt.  Unknown mode: DGEMM_ERR_UNSUPPORTED.
+ */
+int gemm_f32_tc(int mode, int M, int N, int K,
+                const float *A, int lda,
+                const float *B, int ldb,
+                float *C, int ldc,
+                cudaStream_t stream);
+
+/*
+ * gemm_bf16_tc -- BF16 inputs, FP32 accumulate, FP32 output, on tcgen05.
+ *
+ * Lesson 8 section 二十二 lists BF16 among the tensor-core input types; this is
+ * the BF16-in / FP32-accumulate form of gemm_f32_tc.
+ * A: M x K bfloat16 (raw 16-bit patterns), row-major, lda >= max(1, K).
+ * B: K x N bfloat16, row-major, ldb >= max(1, N).
+ * C: M x N fp32, row-major, ldc >= max(1, N); overwritten.
+ * Accuracy: |C - C_exact| <= 8e-3 * (|A| x |B|), C_exact the exact product of
+ * the bf16 values.
+ */
+int gemm_bf16_tc(int M, int N, int K,
+                 const unsigned short *A, int lda,
+                 const unsigned short *B, int ldb,
+                 float *C, int ldc,
+                 cudaStream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char *dgemm_status_string(int status);
+
+/* The CUDA error text behind the calling thread's last DGEMM_ERR_CUDA
+ * ("" if none).  The pointer stays valid until the thread's next call. */
+const char *dgemm_last_cuda_error(void);
+
+/*
+ * dgemm_watchdog_status -- synchronise `stream`, then read and clear the
+ * current device's watchdog word.  The tensor-core kernels bound every wait
+ * on a shared-memory barrier; a wait that runs out (a hardware or library
+ * fault, never expected in normal use) makes the kernel record where it gave
+ * up, drain its copies, free its tensor memory and return, leaving C
+ * incomplete.  Returns DGEMM_OK when no kernel gave up since the last read,
+ * DGEMM_ERR_WATCHDOG when one did (*where, if not NULL, gets the recorded
+ * site code), DGEMM_ERR_CUDA on a CUDA error.
+ */
+int dgemm_watchdog_status(cudaStream_t stream, int *where);
+
+/* Library version as an integer, major*10000 + minor*100 + patch. */
+int dgemm_version(void);
+
+/* Number of kernels this library has launched in this process, on any
+ * device or stream (a diagnostic for counting launches around a region). */
+unsigned long long dgemm_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGEMM_H */

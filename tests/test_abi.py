@@ -1,0 +1,135 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/dgemm.h declares, and rejects invalid calls on the host before any
+CUDA call (the validation order is documented in csrc/api.cu)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_f32_gb300 as dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "dgemm.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(ln for ln in text.splitlines() if not ln.lstrip().startswith("#"))
+    return sorted(set(re.findall(r"(\w+)\s*\([^;{}]*\)\s*;", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_gemm_f32_gb300 import build
+
+    build.build()
+    return dg.load()
+
+
+def test_header_declares_the_documented_entry_points():
+    assert _declared_functions() == sorted(dg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libdgemm.so does not export {name}"
+        ctypes.cast(getattr(lib, name), ctypes.c_void_p)
+
+
+def test_status_strings_and_version(lib):
+    for st in range(0, 10):
+        s = dg.dgemm_status_string(st)
+        assert s and s != "unknown status"
+    assert dg.dgemm_status_string(99) == "unknown status"
+    assert dg.dgemm_version() >= 100
+
+
+P = 0x10000  # a fake, 16-byte aligned address: never dereferenced by these calls
+
+
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+def test_invalid_sizes_rejected(lib, fn):
+    call = _caller(fn)
+    E = dg.ERR_INVALID_VALUE
+    assert call(-1, 4, 4, P, 4, P * 2, 4, P * 3, 4) == E
+    assert call(4, -1, 4, P, 4, P * 2, 4, P * 3, 4) == E
+    assert call(4, 4, -1, P, 4, P * 2, 4, P * 3, 4) == E
+    assert call(4, 4, 8, P, 7, P * 2, 4, P * 3, 4) == E     # lda < K
+    assert call(4, 8, 4, P, 4, P * 2, 7, P * 3, 8) == E     # ldb < N
+    assert call(4, 8, 4, P, 4, P * 2, 8, P * 3, 7) == E     # ldc < N
+    assert call(4, 4, 0, P, 0, P * 2, 4, P * 3, 4) == E     # lda must be >= 1
+
+
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+def test_empty_output_is_a_no_op(lib, fn):
+    call = _caller(fn)
+    # nothing to do: pointers are not looked at, no CUDA call is made
+    assert call(0, 5, 5, 0, 5, 0, 5, 0, 5) == dg.OK
+    assert call(5, 0, 5, 0, 5, 0, 1, 0, 1) == dg.OK
+
+
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+def test_null_pointers_rejected(lib, fn):
+    call = _caller(fn)
+    E = dg.ERR_NULL_POINTER
+    assert call(4, 4, 4, 0, 4, P, 4, P * 4, 4) == E
+    assert call(4, 4, 4, P, 4, 0, 4, P * 4, 4) == E
+    assert call(4, 4, 4, P, 4, P * 2, 4, 0, 4) == E
+    assert call(4, 4, 0, P, 1, P * 2, 4, 0, 4) == E       # K == 0 still writes C
+
+
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+def test_misaligned_pointers_rejected(lib, fn):
+    call = _caller(fn)
+    es = 2 if fn == "bf16" else 4
+    E = dg.ERR_MISALIGNED
+    assert call(4, 4, 4, P + 1, 4, P * 2, 4, P * 4, 4) == E
+    assert call(4, 4, 4, P, 4, P * 2 + 1, 4, P * 4, 4) == E
+    assert call(4, 4, 4, P, 4, P * 2, 4, P * 4 + 2, 4) == E   # C is fp32: 4-byte aligned
+    if es == 4:
+        assert call(4, 4, 4, P + 2, 4, P * 2, 4, P * 4, 4) == E
+
+
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+def test_alias_rejected(lib, fn):
+    call = _caller(fn)
+    es = 2 if fn == "bf16" else 4
+    E = dg.ERR_ALIAS
+    # C starts inside A's span / B's span
+    assert call(8, 8, 8, P, 8, P * 4, 8, P + 8 * 8 * es - 4, 8) == E
+    assert call(8, 8, 8, P, 8, P * 4, 8, P * 4 + 16, 8) == E
+    # A inside C's span
+    assert call(8, 8, 8, P * 4 + 64, 8, P * 8, 8, P * 4, 8) == E
+
+
+def test_unknown_mode_rejected(lib):
+    assert dg.gemm_f32_tc(7, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.gemm_f32_tc(-1, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+
+
+def test_matmul_argument_checks_need_no_gpu():
+    import torch
+
+    with pytest.raises(ValueError):
+        dg.matmul(torch.zeros(2, 3), torch.zeros(3, 2), mode="fp64")
+    with pytest.raises(TypeError):
+        dg.matmul(torch.zeros(2, 3), torch.zeros(3, 2, dtype=torch.float64), mode="simt")
+    with pytest.raises(ValueError):
+        dg.matmul(torch.zeros(2, 3), torch.zeros(4, 2), mode="simt")
+
+
+def test_watchdog_site_codes_documented():
+    src = open(os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc", "tc.cu"), encoding="utf-8").read()
+    codes = re.findall(r"kSite\w+ = (0x[0-9a-f]+)", src)
+    assert len(codes) == len(set(codes)) >= 5
+
+
+def _caller(fn):
+    if fn == "simt":
+        return lambda *a: dg.gemm_f32_simt(*a, 0)
+    if fn == "tf32":
+        return lambda *a: dg.gemm_f32_tc(dg.TC_TF32, *a, 0)
+    if fn == "3xtf32":
+        return lambda *a: dg.gemm_f32_tc(dg.TC_3XTF32, *a, 0)
+    return lambda *a: dg.gemm_bf16_tc(*a, 0)

@@ -1,0 +1,155 @@
+"""Edge cases of every GPU path against the CPU oracle.
+
+Boundary sizes around every tile edge (Lesson 8 section 二十六: partial last
+tiles are zero-filled on load and masked on store), leading dimensions above
+the minimum, operands whose rows are not 16-byte aligned, guard bands around
+C (nothing outside the M x N region may change), K = 0, one-row and
+one-column shapes, long K loops, more tiles than SMs, determinism, and the
+rejection of host pointers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+from dense_gemm_f32_gb300 import inputs
+import dense_gemm_f32_gb300 as dg
+
+pytestmark = pytest.mark.gpu
+
+EDGE = [1, 2, 3, 7, 8, 15, 16, 17, 31, 33, 63, 65, 127, 129, 255, 257]
+# every edge value appears in every dimension, combined with different others
+SWEEP = sorted({(EDGE[i], EDGE[(i + 5) % 16], EDGE[(i + 11) % 16]) for i in range(16)}
+               | {(EDGE[(i + 3) % 16], EDGE[i], EDGE[(i + 7) % 16]) for i in range(16)}
+               | {(EDGE[(i + 9) % 16], EDGE[(i + 2) % 16], EDGE[i]) for i in range(16)})
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    gu.check_watchdog()
+
+
+def _check(mode, A, B, what, Adev=None, Bdev=None, out=None):
+    C = gu.run(mode, A.cuda() if Adev is None else Adev, B.cuda() if Bdev is None else Bdev, out)
+    ref, S = gu.oracle_full(A, B)
+    gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL[mode], what)
+    return C
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_boundary_sweep(mode):
+    for (M, N, K) in SWEEP:
+        A, B = inputs.make_random(M, N, K, seed=M * 1000003 + N * 1009 + K,
+                                  dist="normal", dtype=gu.in_dtype(mode))
+        _check(mode, A, B, f"{mode} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_degenerate_shapes(mode):
+    for (M, N, K) in [(1, 1, 1), (1, 1, 4096), (1, 777, 33), (777, 1, 33), (5, 3, 1),
+                      (129, 257, 1), (1, 4096, 1)]:
+        A, B = inputs.make_random(M, N, K, seed=17, dist="uniform", dtype=gu.in_dtype(mode))
+        _check(mode, A, B, f"{mode} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_long_k_and_many_tiles(mode):
+    """K = 5000 (many pipeline wraps, ragged last k-block) and a 4100 x 2100
+    output (more tiles than SMs, so the persistent CTAs take several tiles
+    and both accumulator buffers)."""
+    A, B = inputs.make_random(130, 270, 5000, seed=23, dtype=gu.in_dtype(mode))
+    _check(mode, A, B, f"{mode} long K")
+    A, B = inputs.make_random(4100, 2100, 100, seed=24, dtype=gu.in_dtype(mode))
+    _check(mode, A, B, f"{mode} many tiles")
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_k_zero_sets_c_to_zero(mode):
+    M, N = 70, 90
+    A = torch.zeros((M, 0), dtype=gu.in_dtype(mode), device="cuda")
+    B = torch.zeros((0, N), dtype=gu.in_dtype(mode), device="cuda")
+    buf, C = gu.guarded_output(M, N, ldc=N + 3)
+    gu.run(mode, A, B, out=C)
+    assert torch.count_nonzero(C).item() == 0
+    gu.assert_guards_intact(buf, M, N, N + 3)
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_leading_dimensions_and_guard_bands(mode):
+    """A, B, C read/written through leading dimensions above the minimum, with
+    NaN in the padding of A and B and a sentinel around and inside C's gaps."""
+    M, N, K = 301, 259, 173
+    A, B = inputs.make_random(M, N, K, seed=31, dist="normal", dtype=gu.in_dtype(mode))
+    for (lda, ldb, ldc) in [(K + 3, N + 5, N + 7), (K + 8, N + 8, N + 8), (2 * K, 2 * N, 3 * N)]:
+        Ad = gu.device_view(*inputs.embed(A, lda))
+        Bd = gu.device_view(*inputs.embed(B, ldb))
+        assert Ad.stride(0) == lda and Bd.stride(0) == ldb
+        buf, C = gu.guarded_output(M, N, ldc)
+        out = gu.run(mode, Ad, Bd, out=C)
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(out.cpu().numpy(), ref, S, gu.TOL[mode], f"{mode} ld {lda},{ldb},{ldc}")
+        gu.assert_guards_intact(buf, M, N, ldc)
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_misaligned_bases(mode):
+    """Base pointers 1..3 elements past a 16-byte boundary (fp32) or 1..7
+    (bf16): not 16-byte aligned, so no 128-bit or TMA access may start there."""
+    M, N, K = 190, 150, 90
+    es = 2 if mode == "bf16" else 4
+    A, B = inputs.make_random(M, N, K, seed=37, dtype=gu.in_dtype(mode))
+    for off in range(1, 16 // es):
+        Ad = gu.device_view(*inputs.embed(A, K, offset=off))
+        Bd = gu.device_view(*inputs.embed(B, N, offset=(off * 3) % (16 // es)))
+        buf = torch.full((1 + M * N + 8,), gu.SENTINEL, dtype=torch.float32, device="cuda")
+        C = buf.as_strided((M, N), (N, 1), 1 + (off % 3))
+        assert Ad.data_ptr() % 16 != 0 and C.data_ptr() % 16 != 0
+        out = gu.run(mode, Ad, Bd, out=C)
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(out.cpu().numpy(), ref, S, gu.TOL[mode], f"{mode} offset {off}")
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_deterministic(mode):
+    A, B = inputs.make_random(1000, 1100, 900, seed=41, dtype=gu.in_dtype(mode))
+    Ad, Bd = A.cuda(), B.cuda()
+    C1 = gu.run(mode, Ad, Bd).clone()
+    C2 = gu.run(mode, Ad, Bd)
+    assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("mode", gu.ALL_MODES)
+def test_host_pointers_rejected(mode):
+    """Host memory (pageable or pinned) is refused before any launch."""
+    A, B = inputs.make_random(64, 64, 64, seed=43, dtype=gu.in_dtype(mode))
+    C = torch.empty((64, 64), dtype=torch.float32, device="cuda")
+    call = {"simt": lambda a, b, c: dg.gemm_f32_simt(64, 64, 64, a, 64, b, 64, c, 64, 0),
+            "tf32": lambda a, b, c: dg.gemm_f32_tc(dg.TC_TF32, 64, 64, 64, a, 64, b, 64, c, 64, 0),
+            "3xtf32": lambda a, b, c: dg.gemm_f32_tc(dg.TC_3XTF32, 64, 64, 64, a, 64, b, 64, c,
+                                                     64, 0),
+            "bf16": lambda a, b, c: dg.gemm_bf16_tc(64, 64, 64, a, 64, b, 64, c, 64, 0)}[mode]
+    Ad, Bd = A.cuda(), B.cuda()
+    assert call(A.data_ptr(), Bd.data_ptr(), C.data_ptr()) == dg.ERR_INVALID_POINTER
+    Bp = B.pin_memory()
+    assert call(Ad.data_ptr(), Bp.data_ptr(), C.data_ptr()) == dg.ERR_INVALID_POINTER
+    Ch = torch.empty((64, 64), dtype=torch.float32)
+    assert call(Ad.data_ptr(), Bd.data_ptr(), Ch.data_ptr()) == dg.ERR_INVALID_POINTER
+
+
+def test_streams_are_honoured():
+    """Work is enqueued on the given stream and ordered with it."""
+    A, B = inputs.make_random(512, 512, 512, seed=47)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        Ad, Bd = A.cuda(non_blocking=False), B.cuda()
+        C = dg.matmul(Ad, Bd, mode="tf32", stream=s)
+        C2 = dg.matmul(Ad, Bd, mode="simt", stream=s)
+    s.synchronize()
+    ref, S = gu.oracle_full(A, B)
+    gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL["tf32"], "tf32 on side stream")
+    gu.assert_close(C2.cpu().numpy(), ref, S, gu.TOL["simt"], "simt on side stream")
