@@ -86,6 +86,15 @@ struct Cfg {
   static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
   static_assert(kSplitWarp0 == kEpiWarp0 + kEpiWarps, "split warps follow the epilogue warps");
 
+  // B (MN-major) layout.  16-bit operands use the plain 128-byte swizzle
+  // (16-byte chunks permuted within each 128-byte row); 32-bit MN-major
+  // operands need the 128-byte swizzle with 32-byte atoms (descriptor layout
+  // type 1, TMA mode SWIZZLE_128B_ATOM_32B).  Rows of a B box are contiguous
+  // 128-byte lines, so the K-group stride is (group rows) x 128 B: 512 B
+  // covers both a 4-row and an 8-row swizzle period for the 8-row MMA slice.
+  static constexpr uint32_t B_LAYOUT = kBF16 ? 2u : 1u;
+  static constexpr uint32_t B_SBO = kBF16 ? 1024u : 512u;
+
   // Instruction descriptor: D fp32, A/B TF32 or BF16, A K-major, B MN-major,
   // N >> 3 at bit 17, M >> 4 at bit 24.
   static constexpr uint32_t IDESC = (1u << 4) | ((kBF16 ? 1u : 2u) << 7) |
@@ -93,12 +102,14 @@ struct Cfg {
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 };
 
-// Shared-memory matrix descriptor for a 128B-swizzled operand tile:
-// start address, leading / stride byte offsets (16-byte units), version 1,
-// base offset 0 (tiles are 1024-byte aligned), swizzle mode 2 = 128B.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of a swizzled operand tile: start address,
+// leading / stride byte offsets (16-byte units), version 1, base offset 0
+// (tiles are 1024-byte aligned), layout type at bits 61-63 (2 = 128-byte
+// swizzle, 1 = 128-byte swizzle with 32-byte atoms).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout = 2u) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm, int &tn) {
@@ -262,12 +273,14 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
             // B: MN-major, advance UMMA_K rows = UMMA_K / 8 atoms of 1024 B.
             const uint32_t a_off = (uint32_t)(k * 32);
             const uint32_t b_off = (uint32_t)(k * (G::UMMA_K / 8) * 1024);
-            const uint64_t ad = sw128_desc(a_tile(stage) + a_off, 16, 1024);
-            const uint64_t bd = sw128_desc(b_tile(stage) + b_off, G::B_BOX_BYTES, 1024);
+            const uint64_t ad = smem_desc(a_tile(stage) + a_off, 16, 1024);
+            const uint64_t bd =
+                smem_desc(b_tile(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
             const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
             if constexpr (G::kSplit) {
-              const uint64_t adl = sw128_desc(a_lo(stage) + a_off, 16, 1024);
-              const uint64_t bdl = sw128_desc(b_lo(stage) + b_off, G::B_BOX_BYTES, 1024);
+              const uint64_t adl = smem_desc(a_lo(stage) + a_off, 16, 1024);
+              const uint64_t bdl =
+                  smem_desc(b_lo(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
               umma_tf32(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32(d_tmem, ad, bdl, G::IDESC, 1u);      // A_hi B_lo
               umma_tf32(d_tmem, ad, bd, G::IDESC, 1u);       // A_hi B_hi
@@ -404,9 +417,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D row-major tensor map: `rows` x `cols` elements, leading dimension `ld`,
-// box of box_cols x box_rows, 128-byte swizzle, zero fill out of range.
+// box of box_cols x box_rows, the given swizzle, zero fill out of range.
 bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es, int64_t rows,
-              int64_t cols, int64_t ld, int box_cols, int box_rows) {
+              int64_t cols, int64_t ld, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -414,7 +427,7 @@ bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es,
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -427,8 +440,11 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   const CUtensorMapDataType dt =
       G::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK)) return cudaErrorInvalidValue;
+  const CUtensorMapSwizzle b_swz =
+      G::kBF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+  if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK, b_swz)) return cudaErrorInvalidValue;
   auto kern = tc_gemm_kernel<KIND, BN>;
   static bool attr_set[64] = {};
   int dev = 0;
