@@ -51,6 +51,10 @@ def parse_args(argv=None):
     p.add_argument("--no-modes", action="store_true", help="headline only, skip the per-mode table")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--shape", default=None,
+                   help="M,N,K: time the headline mode on a seeded uniform[-1,1) workload of this "
+                        "shape instead of the benchmark workload (profiling runs)")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -59,8 +63,12 @@ def parse_args(argv=None):
     return a
 
 
-def workload_for(mode, transformer=False):
+def workload_for(mode, transformer=False, shape=None):
     from dense_gemm_f32_gb300 import inputs
+
+    if shape:
+        M, N, K = (int(x) for x in shape.split(","))
+        return inputs.Workload(f"uniform {M}x{N}x{K}", M, N, K, 3, "uniform", bf16=(mode == "bf16"))
 
     if mode == "bf16":
         return inputs.TRANSFORMER_BF16
@@ -404,7 +412,7 @@ def run_ours(args, dist):
 
     # ---- headline
     mode = args.mode
-    w = workload_for(mode)
+    w = workload_for(mode, shape=args.shape)
     A, B, Ad, Bd = device_inputs(w, mode, device)
     C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
     r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device)
@@ -421,10 +429,15 @@ def run_ours(args, dist):
                 "per_launch_flops": w.flops, "launches_per_step": launches_per_step}
 
     # ---- end to end through the public API with host buffers
-    e2e_ms, h2d, d2h = time_e2e(mode, A, B, max(3, min(args.steps, 20)), 3, dist, device)
-    e2e_steps = max(3, min(args.steps, 20))
-    e2e = aggregate(e2e_ms, dist.world, w.flops, e2e_steps, lambda x: dist.max(x, device))
+    e2e_line = None
     del Ad, Bd, C
+    torch.cuda.empty_cache()
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        e2e_ms, h2d, d2h = time_e2e(mode, A, B, e2e_steps, 3, dist, device)
+        e2e = aggregate(e2e_ms, dist.world, w.flops, e2e_steps, lambda x: dist.max(x, device))
+        e2e_line = {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}
     torch.cuda.empty_cache()
 
     # ---- every other mode, same clocking
@@ -473,8 +486,7 @@ def run_ours(args, dist):
                        "parallelism": "replicas" if dist.world > 1 else "single GPU"},
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "e2e": e2e_line,
             "gpu_launches": r["launches"],
             "clocks": clocks,
             "modes": modes,

@@ -1,0 +1,113 @@
+"""bench.py host logic on the CPU: whole-job aggregation over ranks (gloo,
+world size 2), clock summaries, argument rules, the reference arm's rank
+handling, and the traffic table lookup."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_aggregate_single_rank():
+    r = bench.aggregate(10.0, 1, 2e12, 5, lambda x: x)
+    assert r["ms_per_step"] == pytest.approx(2.0)
+    assert r["value"] == pytest.approx(5 * 2e12 / 1e-2 / 1e12)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, local_ms, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port),
+                       "RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    d = bench.Dist()
+    d.init("gloo")
+    d.barrier()
+    r = bench.aggregate(local_ms[rank], d.world, 1e12, 4, d.max)
+    q.put((rank, r))
+    d.close()
+
+
+def test_aggregate_two_ranks_gloo():
+    """Whole-job value = all ranks' flops over the slowest rank's time."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    local = [8.0, 12.0]
+    ps = [ctx.Process(target=_rank_main, args=(r, 2, port, local, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in range(2))
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in (0, 1):
+        assert out[r]["ms_total"] == pytest.approx(12.0)
+        assert out[r]["value"] == pytest.approx(2 * 1e12 * 4 / 12e-3 / 1e12)
+
+
+def test_clock_summary_inside_windows():
+    rows = [{"t": 10.0, "sm": 1800.0, "max": 2070.0, "reasons": {"sw_power_cap": "Not Active"}},
+            {"t": 10.5, "sm": 2000.0, "max": 2070.0, "reasons": {"sw_power_cap": "Active"}},
+            {"t": 20.0, "sm": 900.0, "max": 2070.0, "reasons": {"hw_slowdown": "Active"}}]
+    c = bench.summarize_clocks(rows, [(9.9, 10.6)])
+    assert c["samples"] == 2 and c["sm_mhz"] == 1900.0
+    assert c["reasons"] == ["sw_power_cap"]
+    c2 = bench.summarize_clocks(rows, [(30.0, 30.1)])
+    assert c2["samples"] == 3
+    assert bench.summarize_clocks([], [(0, 1)])["sm_mhz"] is None
+
+
+def test_args_rules():
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1 and a.impl == "ours"
+
+
+def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_mode_peaks():
+    peaks = {"bf16_tflops": 2000.0, "sm_max_mhz": 2000.0}
+    assert bench.mode_peak("bf16", peaks, 100)[1] == 2000.0
+    assert bench.mode_peak("tf32", peaks, 100)[1] == pytest.approx(2000.0 * 1.1 / 2.25)
+    b, p, _ = bench.mode_peak("simt", peaks, 100)
+    assert b == "alu" and p == pytest.approx(100 * 128 * 2 * 2000e6 / 1e12)
+
+
+def test_traffic_table_respects_source_hash(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    sha = bench.source_sha("tf32")
+    (prof / "dram_traffic.md").write_text(
+        "| mode | workload | source | bytes |\n|---|---|---|---|\n"
+        f"| tf32 | w1 | {sha} | 1234 |\n| simt | w1 | 000000000000 | 99 |\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "dense_gemm_f32_gb300").symlink_to(os.path.join(ROOT, "dense_gemm_f32_gb300"))
+    assert bench.profiled_traffic("tf32", "w1") == 1234.0
+    assert bench.profiled_traffic("simt", "w1") is None
+    assert bench.profiled_traffic("tf32", "other") is None
+
+
+def test_reference_line_shape(capsys):
+    """The reference arm prints one JSON line with the contract's keys (run on
+    a tiny sample: 1 step)."""
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "cpu_baseline", "e2e", "config"):
+        assert k in line
+    assert line["impl"] == "reference" and line["e2e"]["h2d_bytes_per_step"] == 0
