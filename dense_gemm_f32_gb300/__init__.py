@@ -11,9 +11,10 @@ libdgemm.so every call raises.
 """
 from ._lib import (  # noqa: F401  (re-exported C entry points)
     ERR_ALIAS, ERR_ARCH, ERR_CUDA, ERR_INVALID_POINTER, ERR_INVALID_VALUE, ERR_MISALIGNED,
-    ERR_NULL_POINTER, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, LIB_PATH, OK, TC_3XTF32,
+    ERR_NULL_POINTER, ERR_SCRATCH_LIMIT, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, LIB_PATH,
+    NOALLOC_SCRATCH_BYTES, OK, TC_3XTF32,
     TC_TF32, LibraryMissing, dgemm_kernel_launches, dgemm_last_cuda_error, dgemm_status_string, dgemm_version,
-    dgemm_watchdog_status, gemm_bf16_tc, gemm_f32_simt, gemm_f32_tc, load,
+    dgemm_watchdog_status, gemm_bf16_tc, gemm_f32_simt, gemm_f32_tc, gemm_f32_tc_noalloc, load,
 )
 
 MODES = ("simt", "tf32", "3xtf32", "bf16")

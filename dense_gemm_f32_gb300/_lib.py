@@ -21,13 +21,15 @@ ERR_ARCH = 6
 ERR_MISALIGNED = 7
 ERR_INVALID_POINTER = 8
 ERR_WATCHDOG = 9
+ERR_SCRATCH_LIMIT = 10
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 TC_TF32 = 0
 TC_3XTF32 = 1
 
 EXPORTED = ("gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
             "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-            "dgemm_kernel_launches")
+            "dgemm_kernel_launches", "gemm_f32_tc_noalloc")
 
 _lib = None
 
@@ -65,6 +67,8 @@ def load():
     lib.dgemm_version.restype = i
     lib.dgemm_kernel_launches.argtypes = []
     lib.dgemm_kernel_launches.restype = ctypes.c_ulonglong
+    lib.gemm_f32_tc_noalloc.argtypes = [i] + gemm_args
+    lib.gemm_f32_tc_noalloc.restype = i
     _lib = lib
     return lib
 
@@ -75,6 +79,12 @@ def gemm_f32_simt(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
 
 def gemm_f32_tc(mode, M, N, K, A, lda, B, ldb, C, ldc, stream=0):
     return load().gemm_f32_tc(mode, M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f32_tc_noalloc(mode, M, N, K, A, lda, B, ldb, C, ldc, stream=0):
+    """gemm_f32_tc without allocating: re-pitch scratch is the library's fixed
+    16 MiB device array (see include/dgemm.h)."""
+    return load().gemm_f32_tc_noalloc(mode, M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def gemm_bf16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):

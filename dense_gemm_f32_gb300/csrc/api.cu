@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "../../include/dgemm.h"
@@ -176,9 +177,82 @@ done:
   return after_launch(e, "tensor-core GEMM launch");
 }
 
+// ------------------------------------------------------------------------
+// Fixed scratch for gemm_f32_tc_noalloc: the re-pitch target of operands
+// whose rows do not start on 16-byte boundaries, held by every GPU that loads
+// the library.  In host code `g_noalloc_scratch` names a host-side stand-in,
+// not the device array: only the address from cudaGetSymbolAddress (looked
+// up once per device, with that device current) is passed to kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DGEMM_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of this device's scratch array (set-up on first use).
+int noalloc_scratch(int dev, void **ptr) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress (no-alloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return DGEMM_OK;
+}
+
+// run_tc with the fixed scratch array in place of cudaMallocAsync.
+int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda, const float *B,
+                   int ldb, float *C, int ldc, int dev, int num_sms, cudaStream_t stream) {
+  const int es = 4;
+  const int64_t pitch_elems = 16 / es;
+  const void *Ause = A, *Buse = B;
+  int64_t lda_use = lda, ldb_use = ldb;
+  const bool a_ok = tma_ok(A, lda, es), b_ok = tma_ok(B, ldb, es);
+  cudaError_t e = cudaSuccess;
+  if (!a_ok || !b_ok) {
+    const int64_t lda2 = (K + pitch_elems - 1) / pitch_elems * pitch_elems;
+    const int64_t ldb2 = (N + pitch_elems - 1) / pitch_elems * pitch_elems;
+    const uint64_t a_bytes = a_ok ? 0 : ((uint64_t)M * lda2 * es + 255) / 256 * 256;
+    const uint64_t b_bytes = b_ok ? 0 : ((uint64_t)K * ldb2 * es + 255) / 256 * 256;
+    if (a_bytes + b_bytes > (uint64_t)DGEMM_NOALLOC_SCRATCH_BYTES) return DGEMM_ERR_SCRATCH_LIMIT;
+    void *base = nullptr;
+    const int st = noalloc_scratch(dev, &base);
+    if (st != DGEMM_OK) return st;
+    char *s = static_cast<char *>(base);
+    if (!a_ok) {
+      e = dg::launch_repitch(A, lda, s, lda2, M, K, es, num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "re-pitch launch (no-alloc)");
+      Ause = s;
+      lda_use = lda2;
+    }
+    if (!b_ok) {
+      e = dg::launch_repitch(B, ldb, s + a_bytes, ldb2, K, N, es, num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "re-pitch launch (no-alloc)");
+      Buse = s + a_bytes;
+      ldb_use = ldb2;
+    }
+  }
+  e = dg::launch_tc(kind, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
+  return after_launch(e, "tensor-core GEMM launch (no-alloc)");
+}
+
 }  // namespace
 
 extern "C" {
+
+int gemm_f32_tc_noalloc(int mode, int M, int N, int K, const float *A, int lda, const float *B,
+                        int ldb, float *C, int ldc, cudaStream_t stream) {
+  if (mode != DGEMM_TC_TF32 && mode != DGEMM_TC_3XTF32) return DGEMM_ERR_UNSUPPORTED;
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  return run_tc_noalloc(mode == DGEMM_TC_TF32 ? dg::TcKind::kTF32 : dg::TcKind::k3xTF32, M, N, K,
+                        A, lda, B, ldb, C, ldc, dev, sms, stream);
+}
 
 int gemm_f32_simt(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
                   float *C, int ldc, cudaStream_t stream) {
@@ -227,6 +301,9 @@ const char *dgemm_status_string(int status) {
     case DGEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
     case DGEMM_ERR_INVALID_POINTER: return "A, B or C is not device memory of the current device";
     case DGEMM_ERR_WATCHDOG: return "a kernel gave up a bounded wait; its output is incomplete";
+    case DGEMM_ERR_SCRATCH_LIMIT:
+      return "operands need more re-pitch scratch than gemm_f32_tc_noalloc's fixed 16 MiB; "
+             "use gemm_f32_tc";
     default: return "unknown status";
   }
 }

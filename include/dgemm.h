@@ -66,7 +66,8 @@ typedef enum {
     DGEMM_ERR_ARCH = 6,            /* current device is not compute capability 10.3 */
     DGEMM_ERR_MISALIGNED = 7,      /* pointer not aligned to its element size    */
     DGEMM_ERR_INVALID_POINTER = 8, /* A, B or C is not device-accessible memory  */
-    DGEMM_ERR_WATCHDOG = 9         /* a kernel gave up a bounded wait (see dgemm_watchdog_status) */
+    DGEMM_ERR_WATCHDOG = 9,        /* a kernel gave up a bounded wait (see dgemm_watchdog_status) */
+    DGEMM_ERR_SCRATCH_LIMIT = 10   /* gemm_f32_tc_noalloc: operands need more than its fixed scratch */
 } dgemm_status_t;
 
 /* Tensor-core precision modes of gemm_f32_tc. */
@@ -133,6 +134,47 @@ int gemm_bf16_tc(int M, int N, int K,
                  const unsigned short *B, int ldb,
                  float *C, int ldc,
                  cudaStream_t stream);
+
+/*
+ * gemm_f32_tc_noalloc -- gemm_f32_tc for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that must not allocate device memory during the call: code that runs with
+ * every byte of device memory reserved up front (a serving process that has
+ * partitioned HBM among its models, where a new allocation can fail), code
+ * called from inside an allocator or memory-manager callback (which must not
+ * re-enter the allocator), and latency-critical loops that must not risk an
+ * allocation failing or growing a memory pool in the middle of a run.
+ *
+ * Same arguments, semantics, accuracy and status codes as gemm_f32_tc.  The
+ * difference is where the re-pitch scratch lives: gemm_f32_tc takes it from
+ * cudaMallocAsync when A or B rows do not start on 16-byte boundaries; this
+ * entry point uses instead a fixed 16 MiB array (DGEMM_NOALLOC_SCRATCH_BYTES)
+ * that the library holds in device memory on every GPU that loads it, until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *   - Limit: the re-pitched copies of A and/or B (rows rounded up to 16 bytes,
+ *     each copy rounded up to 256 bytes) must fit in 16 MiB; otherwise the
+ *     call returns DGEMM_ERR_SCRATCH_LIMIT and launches nothing.  Operands
+ *     that need no re-pitch use no scratch, at any size.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins on the device.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents.  Each call overwrites all the scratch it reads before
+ *     reading it, so nothing needs clearing; but two calls whose work
+ *     overlaps on the GPU (different streams, no ordering between them) race
+ *     on the array and may corrupt each other's results.  Order such calls
+ *     on one stream or with events.
+ */
+int gemm_f32_tc_noalloc(int mode, int M, int N, int K,
+                        const float *A, int lda,
+                        const float *B, int ldb,
+                        float *C, int ldc,
+                        cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch array gemm_f32_tc_noalloc uses. */
+#define DGEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* Static English text for a status code (never NULL). */
 const char *dgemm_status_string(int status);

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for st in range(0, 10):
+    for st in range(0, 11):
         s = dg.dgemm_status_string(st)
         assert s and s != "unknown status"
     assert dg.dgemm_status_string(99) == "unknown status"
