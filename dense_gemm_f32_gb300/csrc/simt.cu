@@ -1,20 +1,23 @@
 // simt.cu -- FP32 GEMM on the CUDA cores (FFMA), register blocked.
 //
 // The block-tiled, register-blocked SGEMM that "SGEMM 优化旅程" builds up in
-// Levels 2-5, with the sizes its Level 5 names (block tile 128 x 128 x 8,
-// 256 threads, an 8 x 8 register tile per thread), and the structure of
+// Levels 2-5 (shared-memory tiles, padding against bank conflicts, double
+// buffering, a register tile per thread) with the structure of
 // "第八课：GPU 如何完成矩阵乘法": C_tile = sum_t A_tile,t x B_tile,t (section 九),
 // accumulation in registers with one store per element (section 十四),
 // multi-level block / warp / thread tiling (section 十九), double-buffered
 // shared memory (section 二十四), zero-fill and masked stores at the edges
 // (section 二十六), padding against bank conflicts (section 二十七).
 //
+// Shipped shape (chosen by measurement on GB300 over tile shapes, BK, lane
+// orders, unroll depths and packed fma.rn.f32x2 variants): block tile
+// 128 x 256 x 16, 256 threads as 2 x 4 warps of 64 x 64, lanes 8 x 4, an
+// 8 x 16 register tile per thread, one CTA per SM (about 250 registers).
 // GB300 specifics that differ from the pages' kernels:
-//  * A is stored transposed (k-major) in shared memory, so that both operand
-//    fragments are read with 128-bit shared loads; the transposed stores use a
-//    4-float row padding, which makes them bank-conflict free.
-//  * The per-warp tile is 64 x 32 with 8 x 4 lanes, so each 128-bit fragment
-//    load of a warp touches one 128-byte line (one shared-memory wavefront).
+//  * A is stored transposed (k-major) in shared memory so that both operand
+//    fragments are read with 128-bit shared loads; its rows carry a 4-float
+//    pad that keeps the transposed stores free of bank conflicts.
+//  * Every 128-bit fragment load of a warp reads one contiguous line.
 //  * Global loads are 128-bit where the operand rows are 16-byte aligned
 //    (template kVec); ragged edges fall back to masked scalar loads.
 //  * Thread blocks walk the C tiles in groups of 8 tile rows so that panels
@@ -27,9 +30,6 @@
 namespace dg {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 8;
-constexpr int kThreads = 256;
-constexpr int kApad = 4;          // As row = BM + 4 floats (528 B, 16-B multiple)
 constexpr int kGroupM = 8;        // tile rows per raster group
 
 // Load 4 consecutive elements X[r][c..c+3] of an R x Cn row-major matrix,
@@ -52,13 +52,37 @@ __device__ __forceinline__ float4 load4(const float *__restrict__ X, int64_t ld,
   return v;
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kThreads, 2)
+// Block tile BM x BN x BK, WM x WN warps, each warp a (BM/WM) x (BN/WN) tile
+// with its 32 lanes arranged LM x LN; every thread owns TM x TN outputs made
+// of 4 x 4 blocks spaced LM*4 rows and LN*4 columns apart, so that each
+// 128-bit fragment load of a warp reads one contiguous line.
+template <int BM_, int BN_, int BK_, int WM_, int WN_, int LM_, int MIN_BLOCKS_>
+struct SimtCfg {
+  static constexpr int BM = BM_, BN = BN_, BK = BK_, WM = WM_, WN = WN_;
+  static constexpr int LM = LM_, LN = 32 / LM_;
+  static constexpr int AROW = BM + 4;                   // floats per As row (+4 pad)
+  static constexpr int THREADS = WM * WN * 32;
+  static constexpr int TM = BM / WM / LM, TN = BN / WN / LN;
+  static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
+  static constexpr int A_VECS = BM * BK / 4 / THREADS;  // float4 loads of A per thread
+  static constexpr int B_VECS = BK * BN / 4 / THREADS;  // float4 loads of B per thread
+  static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 blocks");
+  static_assert(A_VECS >= 1 && B_VECS >= 1, "every thread loads A and B");
+  static_assert(BM * BK % (4 * THREADS) == 0 && BK * BN % (4 * THREADS) == 0, "even loads");
+  static constexpr int SMEM_BYTES = 2 * BK * AROW * 4 + 2 * BK * BN * 4;  // two buffers
+};
+
+template <class G, bool kVec>
+__global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     sgemm_simt_kernel(int M, int N, int K, const float *__restrict__ A, int64_t lda,
                       const float *__restrict__ B, int64_t ldb, float *__restrict__ C,
                       int64_t ldc, int c_vec) {
-  __shared__ __align__(16) float As[2][BK][BM + kApad];
-  __shared__ __align__(16) float Bs[2][BK][BN];
+  constexpr int BM = G::BM, BN = G::BN, BK = G::BK, TM = G::TM, TN = G::TN;
+  // A stored k-major (transposed): a 128-bit load gives 4 consecutive rows.
+  extern __shared__ float4 simt_smem[];
+  auto As = reinterpret_cast<float(*)[BK][G::AROW]>(simt_smem);
+  auto Bs = reinterpret_cast<float(*)[BK][BN]>(reinterpret_cast<float *>(simt_smem) +
+                                                2 * BK * G::AROW);
 
   // ---- grouped raster: tile id -> (tile row, tile col)
   const int tiles_m = (M + BM - 1) / BM;
@@ -69,90 +93,129 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int first_m = group * kGroupM;
   const int gsize = min(tiles_m - first_m, kGroupM);
   const int in_group = tile - group * per_group;
-  const int tm = first_m + in_group % gsize;
-  const int tn = in_group / gsize;
-  const int m0 = tm * BM, n0 = tn * BN;
+  const int m0 = (first_m + in_group % gsize) * BM;
+  const int n0 = (in_group / gsize) * BN;
 
   const int tid = threadIdx.x;
-  // global -> shared load assignment: one float4 of A and one of B per thread
-  const int a_row = tid >> 1, a_col = (tid & 1) * 4;     // A tile 128 x 8
-  const int b_row = tid >> 5, b_col = (tid & 31) * 4;    // B tile 8 x 128
-
-  // compute assignment: warp tile 64 x 32, lanes 8 (M) x 4 (N), thread 8 x 8
   const int warp = tid >> 5, lane = tid & 31;
-  const int wm = warp >> 2, wn = warp & 3;               // 2 x 4 warps
-  const int lm = lane >> 2, ln = lane & 3;
-  const int row_base = wm * 64 + lm * 4;                 // rows row_base + {0..3, 32..35}
-  const int col_base = wn * 32 + ln * 4;                 // cols col_base + {0..3, 16..19}
+  const int wm = warp / G::WN, wn = warp % G::WN;
+  const int lm = lane / G::LN, ln = lane % G::LN;
+  const int row_base = wm * (BM / G::WM) + lm * 4;   // + c * LM * 4, c < TM / 4
+  const int col_base = wn * (BN / G::WN) + ln * 4;   // + c * LN * 4, c < TN / 4
 
-  float acc[8][8];
+  float acc[TM][TN];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+  // global -> shared assignment: A as BM rows x BK/4 float4s, B as BK rows x BN/4
+  float4 ra[G::A_VECS], rb[G::B_VECS];
+  auto load_tiles = [&](int k0) {
+#pragma unroll
+    for (int v = 0; v < G::A_VECS; ++v) {
+      const int e = tid + v * G::THREADS;
+      ra[v] = load4<kVec>(A, lda, m0 + e / (BK / 4), k0 + (e % (BK / 4)) * 4, M, K);
+    }
+#pragma unroll
+    for (int v = 0; v < G::B_VECS; ++v) {
+      const int e = tid + v * G::THREADS;
+      rb[v] = load4<kVec>(B, ldb, k0 + e / (BN / 4), n0 + (e % (BN / 4)) * 4, K, N);
+    }
+  };
+  auto store_tiles = [&](int buf) {
+#pragma unroll
+    for (int v = 0; v < G::A_VECS; ++v) {
+      const int e = tid + v * G::THREADS;
+      const int r = e / (BK / 4), c = (e % (BK / 4)) * 4;
+      As[buf][c + 0][r] = ra[v].x;
+      As[buf][c + 1][r] = ra[v].y;
+      As[buf][c + 2][r] = ra[v].z;
+      As[buf][c + 3][r] = ra[v].w;
+    }
+#pragma unroll
+    for (int v = 0; v < G::B_VECS; ++v) {
+      const int e = tid + v * G::THREADS;
+      *reinterpret_cast<float4 *>(&Bs[buf][e / (BN / 4)][(e % (BN / 4)) * 4]) = rb[v];
+    }
+  };
 
   const int KT = (K + BK - 1) / BK;
-
-  float4 ra = load4<kVec>(A, lda, m0 + a_row, a_col, M, K);
-  float4 rb = load4<kVec>(B, ldb, b_row, n0 + b_col, K, N);
-  As[0][a_col + 0][a_row] = ra.x;
-  As[0][a_col + 1][a_row] = ra.y;
-  As[0][a_col + 2][a_row] = ra.z;
-  As[0][a_col + 3][a_row] = ra.w;
-  *reinterpret_cast<float4 *>(&Bs[0][b_row][b_col]) = rb;
+  load_tiles(0);
+  store_tiles(0);
   __syncthreads();
 
   for (int kt = 0; kt < KT; ++kt) {
     const int cur = kt & 1;
     const bool more = kt + 1 < KT;
-    if (more) {
-      const int k0 = (kt + 1) * BK;
-      ra = load4<kVec>(A, lda, m0 + a_row, k0 + a_col, M, K);
-      rb = load4<kVec>(B, ldb, k0 + b_row, n0 + b_col, K, N);
-    }
+    if (more) load_tiles((kt + 1) * BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][row_base]);
-      const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][row_base + 32]);
-      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][col_base]);
-      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][col_base + 16]);
-      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      float a[TM], b[TN];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int c = 0; c < TM / 4; ++c) {
+        const float4 v =
+            *reinterpret_cast<const float4 *>(&As[cur][kk][row_base + c * G::LM * 4]);
+        a[4 * c] = v.x, a[4 * c + 1] = v.y, a[4 * c + 2] = v.z, a[4 * c + 3] = v.w;
+      }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      for (int c = 0; c < TN / 4; ++c) {
+        const float4 v =
+            *reinterpret_cast<const float4 *>(&Bs[cur][kk][col_base + c * G::LN * 4]);
+        b[4 * c] = v.x, b[4 * c + 1] = v.y, b[4 * c + 2] = v.z, b[4 * c + 3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
-    if (more) {
-      const int nxt = cur ^ 1;
-      As[nxt][a_col + 0][a_row] = ra.x;
-      As[nxt][a_col + 1][a_row] = ra.y;
-      As[nxt][a_col + 2][a_row] = ra.z;
-      As[nxt][a_col + 3][a_row] = ra.w;
-      *reinterpret_cast<float4 *>(&Bs[nxt][b_row][b_col]) = rb;
-    }
+    if (more) store_tiles(cur ^ 1);
     __syncthreads();
   }
 
   // ---- epilogue: masked stores, 128-bit where C rows are 16-byte aligned
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = m0 + row_base + (i & 3) + (i >> 2) * 32;
+  for (int i = 0; i < TM; ++i) {
+    const int r = m0 + row_base + (i / 4) * G::LM * 4 + (i % 4);
     if (r >= M) continue;
     float *crow = C + (int64_t)r * ldc;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = n0 + col_base + h * 16;
-      const float *v = &acc[i][h * 4];
+    for (int h = 0; h < TN / 4; ++h) {
+      const int c = n0 + col_base + h * G::LN * 4;
+      const float *w = &acc[i][h * 4];
       if (c_vec && c + 3 < N) {
-        *reinterpret_cast<float4 *>(crow + c) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4 *>(crow + c) = make_float4(w[0], w[1], w[2], w[3]);
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (c + j < N) crow[c + j] = v[j];
+          if (c + j < N) crow[c + j] = w[j];
       }
     }
   }
+}
+
+template <class G>
+cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, const float *B,
+                            int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
+                            cudaStream_t stream) {
+  const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
+  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+  auto kern = ab_vec ? sgemm_simt_kernel<G, true> : sgemm_simt_kernel<G, false>;
+  if (G::SMEM_BYTES > 48 * 1024) {
+    // opt in to more than 48 KB of dynamic shared memory (per device, once)
+    static bool done[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !done[ab_vec][dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) done[ab_vec][dev] = true;
+    }
+  }
+  kern<<<(unsigned)tiles, G::THREADS, G::SMEM_BYTES, stream>>>(M, N, K, A, lda, B, ldb, C, ldc,
+                                                               c_vec);
+  return cudaGetLastError();
 }
 
 __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ldc) {
@@ -166,17 +229,14 @@ __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ld
 
 }  // namespace
 
+// The configuration the library ships (see the variant table in the design doc).
+using SimtShipped = SimtCfg<128, 256, 16, 2, 4, 8, 1>;
+
 cudaError_t launch_simt(int M, int N, int K, const float *A, int64_t lda, const float *B,
                         int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
                         cudaStream_t stream) {
-  const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)tiles), block(kThreads);
-  if (ab_vec)
-    sgemm_simt_kernel<true><<<grid, block, 0, stream>>>(M, N, K, A, lda, B, ldb, C, ldc, c_vec);
-  else
-    sgemm_simt_kernel<false><<<grid, block, 0, stream>>>(M, N, K, A, lda, B, ldb, C, ldc, c_vec);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      launch_simt_cfg<SimtShipped>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, stream);
   if (e == cudaSuccess) count_launch();
   return e;
 }

@@ -9,7 +9,8 @@
 //
 // Blackwell design (none of this is on the pages, which stop at WMMA):
 //  * Persistent kernel, one CTA per SM, walking 128 x BN output tiles in
-//    groups of kGroupM tile rows (L2 reuse of the A and B panels).
+//    groups of 32 tile rows (L2 reuse of the A and B panels; measured best of
+//    4, 8, 16 and 32 on GB300 for both TF32 and BF16).
 //  * Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma (one
 //    thread) and owns the TMEM allocation, warps 2-5 drain the accumulator
 //    (tcgen05.ld -> registers -> global).  For 3xTF32, warps 6-9 split each
@@ -25,6 +26,7 @@
 //    the device watchdog word, drains what it issued, frees TMEM and returns.
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -39,7 +41,6 @@ __device__ int g_watchdog = 0;
 
 namespace {
 
-constexpr int kGroupM = 8;
 constexpr int BM = 128;
 
 // Watchdog site codes (role * 16 + place).
@@ -112,11 +113,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &tm, int &tn) {
-  const int per_group = kGroupM * tiles_n;
+// Tile id -> (tile row, tile col): tiles are walked in groups of `group_m`
+// tile rows, column by column inside a group, so that the CTAs working at the
+// same time share A row panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
+                                            int &tm, int &tn) {
+  const int per_group = group_m * tiles_n;
   const int group = tile / per_group;
-  const int first = group * kGroupM;
-  const int gsize = min(tiles_m - first, kGroupM);
+  const int first = group * group_m;
+  const int gsize = min(tiles_m - first, group_m);
   const int r = tile - group * per_group;
   tm = first + r % gsize;
   tn = r / gsize;
@@ -142,7 +147,7 @@ template <TcKind KIND, int BN>
 __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
-                   int N, int K, int64_t ldc, int c_vec) {
+                   int N, int K, int64_t ldc, int c_vec, int group_m) {
   using G = Cfg<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         int tm, tn;
-        tile_coords(tile, tiles_m, tiles_n, tm, tn);
+        tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
             if (!*abort_flag) watchdog_trip(kSiteProducerEmpty, abort_flag);
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int tm, tn;
-      tile_coords(tile, tiles_m, tiles_n, tm, tn);
+      tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
       // every lane waits, so that each one acquires the accumulator itself
       bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
       if (!ok && lane == 0 && !*abort_flag) watchdog_trip(kSiteEpiAccFull, abort_flag);
@@ -432,6 +437,17 @@ bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es,
   return r == CUDA_SUCCESS;
 }
 
+// Tile rows per raster group.  DGEMM_TC_GROUP_M (1..64) overrides the
+// default for tuning sweeps; it changes only the order tiles are visited in.
+int raster_group_m() {
+  static const int g = [] {
+    const char *e = getenv("DGEMM_TC_GROUP_M");
+    const int v = e ? atoi(e) : 0;
+    return (v >= 1 && v <= 64) ? v : 32;
+  }();
+  return g;
+}
+
 template <TcKind KIND, int BN>
 cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
@@ -458,7 +474,8 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0);
+  kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
+                                                     raster_group_m());
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
