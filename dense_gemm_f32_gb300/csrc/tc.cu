@@ -407,6 +407,285 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
   }
 }
 
+// ===================================================================
+// CTA-pair variant (cta_group::2) for TF32 and BF16.
+//
+// A cluster of two CTAs on two SMs computes a 256 x 256 tile.  CTA r loads
+// rows [128 r, 128 r + 128) of the A panel and columns [128 r, 128 r + 128)
+// of the B panel into its own shared memory; one thread of the even CTA
+// issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which reads both halves
+// of both operands and writes rows [128 r, 128 r + 128) of the accumulator
+// into CTA r's tensor memory.  Per SM this halves the B bytes fetched per
+// flop compared with the single-CTA 128 x 256 tile.
+//  * Both CTAs' TMA loads signal the even CTA's full barrier (pair TMA); its
+//    producer posts the expected bytes of both halves.
+//  * The MMA thread's commits arrive on the barrier at the same offset in
+//    both CTAs (multicast): stage-free and accumulator-ready.
+//  * Each CTA's epilogue reads its own TMEM rows; the odd CTA's epilogue
+//    releases the accumulator on the even CTA's barrier.
+//  * Before leaving, each CTA waits (bounded) for every signal still heading
+//    its way, then both CTAs meet at a cluster barrier and free TMEM.
+template <TcKind KIND>
+struct Cfg2 {
+  static constexpr bool kBF16 = KIND == TcKind::kBF16;
+  static constexpr int BM = 256, BN = 256;           // pair tile
+  static constexpr int HM = 128, HN = 128;           // per-CTA halves
+  static constexpr int ES = kBF16 ? 2 : 4;
+  static constexpr int BK = 128 / ES;
+  static constexpr int UMMA_K = 32 / ES;
+  static constexpr int KSTEPS = BK / UMMA_K;
+  static constexpr int BOX_N = 128 / ES;
+  static constexpr int B_BOXES = HN / BOX_N;
+  static constexpr int A_BYTES = HM * 128;
+  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // per CTA
+  static constexpr int STAGES = 196608 / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 512;                   // two 256-column accumulators
+  static constexpr int kEpiWarps = 4;
+  static constexpr int THREADS = 32 * (2 + kEpiWarps);
+  static constexpr int NUM_BARS = 2 * STAGES + 5;         // full, empty, accf[2], acce[2], drain
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
+  static constexpr uint32_t B_LAYOUT = kBF16 ? 2u : 1u;
+  static constexpr uint32_t B_SBO = kBF16 ? 1024u : 512u;
+  static constexpr uint32_t IDESC = (1u << 4) | ((kBF16 ? 1u : 2u) << 7) |
+                                    ((kBF16 ? 1u : 2u) << 10) | (0u << 15) | (1u << 16) |
+                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  static_assert(STAGES >= 2, "pipeline needs at least two stages");
+};
+
+enum : int {
+  kSite2ProducerEmpty = 0x51,
+  kSite2ProducerTail = 0x52,
+  kSite2MmaFull = 0x61,
+  kSite2MmaAccEmpty = 0x62,
+  kSite2MmaDrain = 0x63,
+  kSite2MmaTail = 0x64,
+  kSite2EpiAccFull = 0x71,
+};
+
+template <TcKind KIND>
+__global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
+                    int N, int K, int64_t ldc, int c_vec, int group_m) {
+  using G = Cfg2<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+
+  const uint32_t bars = base + G::STAGES * G::STAGE_BYTES;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (G::STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * G::STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * G::STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * G::STAGES + 4);
+  uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::NUM_BARS * 8;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
+  auto a_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES); };
+  auto b_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES + G::A_BYTES); };
+
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+  const int tiles_m = (M + G::BM - 1) / G::BM;
+  const int tiles_n = (N + G::BN - 1) / G::BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int kblocks = (K + G::BK - 1) / G::BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 2 * G::kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(tmem_slot)), G::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // the peer's barriers are initialised before any signal crosses
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
+        int tm, tn;
+        tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+            if (!*abort_flag) watchdog_trip(kSite2ProducerEmpty, abort_flag);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (uint32_t)G::STAGE_BYTES);
+          tma_load_2d_pair(a_tile(stage), &tmap_a, fb, kb * G::BK, tm * G::BM + rank * G::HM);
+#pragma unroll
+          for (int j = 0; j < G::B_BOXES; ++j)
+            tma_load_2d_pair(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, fb,
+                             tn * G::BN + rank * G::HN + j * G::BOX_N, kb * G::BK);
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Tail: wait until the MMAs have released every stage loaded here, so
+      // that all stage-free signals aimed at this CTA have landed (and, on an
+      // abort, that no copy is still writing this CTA's shared memory).
+      for (int i = 0; i < G::STAGES; ++i) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
+          atomicCAS(&g_watchdog, 0, kSite2ProducerTail);
+          break;
+        }
+        if (++stage == G::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA (even CTA only)
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
+        if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
+          if (!*abort_flag) watchdog_trip(kSite2MmaAccEmpty, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * G::BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+            if (!*abort_flag) watchdog_trip(kSite2MmaFull, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < G::KSTEPS; ++k) {
+            const uint64_t ad = smem_desc(a_tile(stage) + (uint32_t)(k * 32), 16, 1024);
+            const uint64_t bd = smem_desc(b_tile(stage) + (uint32_t)(k * (G::UMMA_K / 8) * 1024),
+                                          G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+            const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+            if constexpr (G::kBF16)
+              umma_f16_pair(d_tmem, ad, bd, G::IDESC, accum);
+            else
+              umma_tf32_pair(d_tmem, ad, bd, G::IDESC, accum);
+          }
+          umma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+          if (++stage == G::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(accf_bar(acc), 0x3);  // accumulator ready in both CTAs
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit_pair(drain_bar, 0x1);
+      if (!mbar_wait(drain_bar, 0)) atomicCAS(&g_watchdog, 0, kSite2MmaDrain);
+      // Tail: both accumulators released by both epilogues, so that every
+      // release signal from the odd CTA has landed before this CTA leaves.
+      for (int i = 0; i < 2; ++i) {
+        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
+          atomicCAS(&g_watchdog, 0, kSite2MmaTail);
+          break;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster; tile < num_tiles; tile += clusters) {
+      int tm, tn;
+      tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+      bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
+      if (!ok && lane == 0 && !*abort_flag) watchdog_trip(kSite2EpiAccFull, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row = tm * G::BM + (int)rank * G::HM + quarter * 32 + lane;
+      float *crow = C + (int64_t)row * ldc;
+      const uint32_t t_row =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * G::BN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < G::BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
+        tmem_wait_ld();
+        const int col = tn * G::BN + c0;
+        if (row < M) {
+          if (c_vec && col + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4 *>(crow + col + j) =
+                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col + j < N) crow[col + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? acce_leader1 : acce_leader0);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // neither CTA leaves while the other may still signal it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -481,6 +760,66 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   return e;
 }
 
+template <TcKind KIND>
+cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const void *B,
+                        int64_t ldb, float *C, int64_t ldc, bool c_vec, cudaStream_t stream) {
+  using G = Cfg2<KIND>;
+  const CUtensorMapDataType dt =
+      G::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle b_swz =
+      G::kBF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, G::HM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK, b_swz)) return cudaErrorInvalidValue;
+  auto kern = tc2_gemm_kernel<KIND>;
+  static int max_clusters[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(G::THREADS);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int maxc = (dev >= 0 && dev < 64) ? max_clusters[dev] : 0;
+  if (maxc == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2);
+    e = cudaOccupancyMaxActiveClusters(&maxc, (void *)kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (maxc < 1) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) max_clusters[dev] = maxc;
+  }
+  const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
+  if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
+  const int clusters = (int)(tiles < maxc ? tiles : maxc);
+  cfg.gridDim = dim3(2 * clusters);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m());
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+// Pair kernel or single-CTA kernel.  DGEMM_TC_PAIR=0 / =1 forces one of them
+// (read on every call, for tests and tuning); by default the pair kernel runs
+// once there are enough 256 x 256 tiles to occupy at least a quarter of the
+// SMs, since it has half as many tiles as the single-CTA kernel.
+bool use_pair(int M, int N, int num_sms) {
+  const char *e = getenv("DGEMM_TC_PAIR");
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  const int64_t pair_tiles = (int64_t)((M + 255) / 256) * ((N + 255) / 256);
+  return pair_tiles * 4 >= num_sms;
+}
+
 __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_bytes,
                                uint8_t *__restrict__ dst, int64_t ldd_bytes, int rows,
                                int64_t row_bytes, int64_t pad_bytes, int es) {
@@ -513,12 +852,16 @@ cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t l
                       int num_sms, cudaStream_t stream) {
   switch (kind) {
     case TcKind::kTF32:
+      if (use_pair(M, N, num_sms))
+        return launch_cfg2<TcKind::kTF32>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
       return launch_cfg<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                             stream);
     case TcKind::k3xTF32:
       return launch_cfg<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                               stream);
     case TcKind::kBF16:
+      if (use_pair(M, N, num_sms))
+        return launch_cfg2<TcKind::kBF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
       return launch_cfg<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                             stream);
   }
