@@ -9,8 +9,7 @@
 //
 // Blackwell design (none of this is on the pages, which stop at WMMA):
 //  * Persistent kernel, one CTA per SM, walking 128 x BN output tiles in
-//    groups of 32 tile rows (L2 reuse of the A and B panels; measured best of
-//    4, 8, 16 and 32 on GB300 for both TF32 and BF16).
+//    groups of tile rows (L2 reuse of the A and B panels; see raster_group_m).
 //  * Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma (one
 //    thread) and owns the TMEM allocation, warps 2-5 drain the accumulator
 //    (tcgen05.ld -> registers -> global).  For 3xTF32, warps 6-9 split each
@@ -428,6 +427,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
 template <TcKind KIND>
 struct Cfg2 {
   static constexpr bool kBF16 = KIND == TcKind::kBF16;
+  static constexpr bool kSplit = KIND == TcKind::k3xTF32;
   static constexpr int BM = 256, BN = 256;           // pair tile
   static constexpr int HM = 128, HN = 128;           // per-CTA halves
   static constexpr int ES = kBF16 ? 2 : 4;
@@ -439,12 +439,15 @@ struct Cfg2 {
   static constexpr int A_BYTES = HM * 128;
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // per CTA
+  static constexpr int RAW_BYTES = A_BYTES + B_BYTES;                // per CTA, per stage
+  static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);   // + lo copies (3xTF32)
   static constexpr int STAGES = 196608 / STAGE_BYTES;
   static constexpr int TMEM_COLS = 512;                   // two 256-column accumulators
   static constexpr int kEpiWarps = 4;
-  static constexpr int THREADS = 32 * (2 + kEpiWarps);
-  static constexpr int NUM_BARS = 2 * STAGES + 5;         // full, empty, accf[2], acce[2], drain
+  static constexpr int kSplitWarp0 = 6, kSplitWarps = kSplit ? 4 : 0;
+  static constexpr int THREADS = 32 * (2 + kEpiWarps + kSplitWarps);
+  // full, empty, ready (3xTF32), accf[2], acce[2], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
   static constexpr uint32_t B_LAYOUT = kBF16 ? 2u : 1u;
   static constexpr uint32_t B_SBO = kBF16 ? 1024u : 512u;
@@ -452,6 +455,7 @@ struct Cfg2 {
                                     ((kBF16 ? 1u : 2u) << 10) | (0u << 15) | (1u << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
+  static_assert(kSplitWarp0 == 2 + kEpiWarps, "split warps follow the epilogue warps");
 };
 
 enum : int {
@@ -462,6 +466,7 @@ enum : int {
   kSite2MmaDrain = 0x63,
   kSite2MmaTail = 0x64,
   kSite2EpiAccFull = 0x71,
+  kSite2SplitFull = 0x81,
 };
 
 template <TcKind KIND>
@@ -478,14 +483,17 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
   const uint32_t bars = base + G::STAGES * G::STAGE_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (G::STAGES + s); };
-  auto accf_bar = [&](int b) { return bars + 8u * (2 * G::STAGES + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (2 * G::STAGES + 2 + b); };
-  const uint32_t drain_bar = bars + 8u * (2 * G::STAGES + 4);
+  auto ready_bar = [&](int s) { return bars + 8u * (2 * G::STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
   uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::NUM_BARS * 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
   auto a_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES); };
   auto b_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES + G::A_BYTES); };
+  auto a_lo = [&](int s) { return a_tile(s) + (uint32_t)G::RAW_BYTES; };
+  auto b_lo = [&](int s) { return b_tile(s) + (uint32_t)G::RAW_BYTES; };
 
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
@@ -500,6 +508,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
     for (int s = 0; s < G::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), G::kSplit ? 2 * G::kSplitWarps : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -539,13 +548,26 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (uint32_t)G::STAGE_BYTES);
-          tma_load_2d_pair(a_tile(stage), &tmap_a, fb, kb * G::BK, tm * G::BM + rank * G::HM);
+          const int ya = tm * G::BM + (int)rank * G::HM;
+          const int xb = tn * G::BN + (int)rank * G::HN;
+          if constexpr (G::kSplit) {
+            // each CTA's split warps wait on its own full barrier
+            mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
+            tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, ya);
 #pragma unroll
-          for (int j = 0; j < G::B_BOXES; ++j)
-            tma_load_2d_pair(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, fb,
-                             tn * G::BN + rank * G::HN + j * G::BOX_N, kb * G::BK);
+            for (int j = 0; j < G::B_BOXES; ++j)
+              tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
+                          xb + j * G::BOX_N, kb * G::BK);
+          } else {
+            // both halves signal the even CTA's full barrier
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (uint32_t)G::RAW_BYTES);
+            tma_load_2d_pair(a_tile(stage), &tmap_a, fb, kb * G::BK, ya);
+#pragma unroll
+            for (int j = 0; j < G::B_BOXES; ++j)
+              tma_load_2d_pair(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, fb, xb + j * G::BOX_N,
+                               kb * G::BK);
+          }
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -583,7 +605,8 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * G::BN);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+          const uint32_t ready = G::kSplit ? ready_bar(stage) : full_bar(stage);
+          if (*abort_flag || !mbar_wait(ready, phase)) {
             if (!*abort_flag) watchdog_trip(kSite2MmaFull, abort_flag);
             ok = false;
             break;
@@ -591,14 +614,24 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < G::KSTEPS; ++k) {
-            const uint64_t ad = smem_desc(a_tile(stage) + (uint32_t)(k * 32), 16, 1024);
-            const uint64_t bd = smem_desc(b_tile(stage) + (uint32_t)(k * (G::UMMA_K / 8) * 1024),
-                                          G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+            const uint32_t a_off = (uint32_t)(k * 32);
+            const uint32_t b_off = (uint32_t)(k * (G::UMMA_K / 8) * 1024);
+            const uint64_t ad = smem_desc(a_tile(stage) + a_off, 16, 1024);
+            const uint64_t bd =
+                smem_desc(b_tile(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
             const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
-            if constexpr (G::kBF16)
+            if constexpr (G::kSplit) {
+              const uint64_t adl = smem_desc(a_lo(stage) + a_off, 16, 1024);
+              const uint64_t bdl =
+                  smem_desc(b_lo(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+              umma_tf32_pair(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
+              umma_tf32_pair(d_tmem, ad, bdl, G::IDESC, 1u);     // A_hi B_lo
+              umma_tf32_pair(d_tmem, ad, bd, G::IDESC, 1u);      // A_hi B_hi
+            } else if constexpr (G::kBF16) {
               umma_f16_pair(d_tmem, ad, bd, G::IDESC, accum);
-            else
+            } else {
               umma_tf32_pair(d_tmem, ad, bd, G::IDESC, accum);
+            }
           }
           umma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == G::STAGES) {
@@ -628,7 +661,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 2 + G::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
@@ -674,6 +707,43 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+  } else if constexpr (G::kSplit) {
+    // ------------------------------------- 3xTF32 split warps (both CTAs)
+    // Split this CTA's staged tiles into hi (in place) and lo, then release
+    // the stage on the even CTA's ready barrier (4 warps x 2 CTAs).
+    const int t = threadIdx.x - 32 * G::kSplitWarp0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        bool got = !*abort_flag && mbar_wait(full_bar(stage), phase);
+        if (!got && lane == 0 && !*abort_flag) watchdog_trip(kSite2SplitFull, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint4 *raw = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES);
+        uint4 *lo = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES + G::RAW_BYTES);
+        for (int i = t; i < G::RAW_BYTES / 16; i += 32 * G::kSplitWarps) {
+          const uint4 v = raw[i];
+          uint4 h, l;
+          split_tf32(__uint_as_float(v.x), h.x, l.x);
+          split_tf32(__uint_as_float(v.y), h.y, l.y);
+          split_tf32(__uint_as_float(v.z), h.z, l.z);
+          split_tf32(__uint_as_float(v.w), h.w, l.w);
+          raw[i] = h;
+          lo[i] = l;
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(ready_bar(stage), 0));
+        if (++stage == G::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -716,15 +786,18 @@ bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es,
   return r == CUDA_SUCCESS;
 }
 
-// Tile rows per raster group.  DGEMM_TC_GROUP_M (1..64) overrides the
-// default for tuning sweeps; it changes only the order tiles are visited in.
-int raster_group_m() {
+// Tile rows per raster group: `dflt` unless DGEMM_TC_GROUP_M (1..64)
+// overrides it for tuning sweeps; it changes only the order tiles are visited
+// in.  Measured best on GB300: 32 rows of 128-row tiles for the single-CTA
+// kernel, 16 rows of 256-row tiles for the pair kernel (4096 A rows per group
+// either way).
+int raster_group_m(int dflt) {
   static const int g = [] {
     const char *e = getenv("DGEMM_TC_GROUP_M");
     const int v = e ? atoi(e) : 0;
-    return (v >= 1 && v <= 64) ? v : 32;
+    return (v >= 1 && v <= 64) ? v : 0;
   }();
-  return g;
+  return g ? g : dflt;
 }
 
 template <TcKind KIND, int BN>
@@ -754,7 +827,7 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
   kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                     raster_group_m());
+                                                     raster_group_m(32));
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
@@ -802,7 +875,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   cfg.gridDim = dim3(2 * clusters);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m());
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m(16));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
@@ -857,6 +930,8 @@ cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t l
       return launch_cfg<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                             stream);
     case TcKind::k3xTF32:
+      if (use_pair(M, N, num_sms))
+        return launch_cfg2<TcKind::k3xTF32>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
       return launch_cfg<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                               stream);
     case TcKind::kBF16:
