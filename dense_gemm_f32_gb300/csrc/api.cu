@@ -263,8 +263,9 @@ int gemm_f32_simt(int M, int N, int K, const float *A, int lda, const float *B, 
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
   const bool ab_vec = aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0;
   const bool c_vec = aligned(C, 16) && ldc % 4 == 0;
-  return after_launch(dg::launch_simt(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, stream),
-                      "SIMT GEMM launch");
+  return after_launch(
+      dg::launch_simt(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, sms, stream),
+      "SIMT GEMM launch");
 }
 
 int gemm_f32_tc(int mode, int M, int N, int K, const float *A, int lda, const float *B, int ldb,

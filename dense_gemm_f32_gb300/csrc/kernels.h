@@ -8,8 +8,11 @@ namespace dg {
 
 // FP32 FFMA GEMM.  ab_vec: A and B rows start on 16-byte boundaries (base
 // pointers 16-byte aligned, lda % 4 == 0, ldb % 4 == 0).  c_vec: same for C.
+// When the output tiles leave a last wave at most half full, those tiles
+// are split along K (partials in stream-ordered scratch, summed in a fixed
+// order by the last part to finish).
 cudaError_t launch_simt(int M, int N, int K, const float *A, int64_t lda, const float *B,
-                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
+                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec, int num_sms,
                         cudaStream_t stream);
 
 // C[i*ldc + j] = 0 for i < M, j < N (the empty sum, K == 0).

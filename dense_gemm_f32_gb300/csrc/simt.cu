@@ -76,7 +76,8 @@ template <class G, bool kVec>
 __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     sgemm_simt_kernel(int M, int N, int K, const float *__restrict__ A, int64_t lda,
                       const float *__restrict__ B, int64_t ldb, float *__restrict__ C,
-                      int64_t ldc, int c_vec) {
+                      int64_t ldc, int c_vec, int split_first, int split_parts,
+                      float *__restrict__ work, unsigned int *__restrict__ counters) {
   constexpr int BM = G::BM, BN = G::BN, BK = G::BK, TM = G::TM, TN = G::TN;
   // A stored k-major (transposed): a 128-bit load gives 4 consecutive rows.
   extern __shared__ float4 simt_smem[];
@@ -84,10 +85,24 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   auto Bs = reinterpret_cast<float(*)[BK][BN]>(reinterpret_cast<float *>(simt_smem) +
                                                 2 * BK * G::AROW);
 
+  // ---- work unit -> (tile, K range).  Blocks below split_first each own a
+  // whole tile; the tiles from split_first on (the last, partial wave) are
+  // each split along K into split_parts parts, one block per part.
+  const int KT = (K + BK - 1) / BK;
+  const bool split = split_parts > 1 && (int)blockIdx.x >= split_first;
+  int tile = blockIdx.x, part = 0, kt_begin = 0, kt_end = KT;
+  if (split) {
+    const int u = blockIdx.x - split_first;
+    tile = split_first + u / split_parts;
+    part = u % split_parts;
+    const int per = (KT + split_parts - 1) / split_parts;
+    kt_begin = min(KT, part * per);
+    kt_end = min(KT, kt_begin + per);
+  }
+
   // ---- grouped raster: tile id -> (tile row, tile col)
   const int tiles_m = (M + BM - 1) / BM;
   const int tiles_n = (N + BN - 1) / BN;
-  const int tile = blockIdx.x;
   const int per_group = kGroupM * tiles_n;
   const int group = tile / per_group;
   const int first_m = group * kGroupM;
@@ -140,14 +155,13 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     }
   };
 
-  const int KT = (K + BK - 1) / BK;
-  load_tiles(0);
+  load_tiles(kt_begin * BK);
   store_tiles(0);
   __syncthreads();
 
-  for (int kt = 0; kt < KT; ++kt) {
-    const int cur = kt & 1;
-    const bool more = kt + 1 < KT;
+  for (int kt = kt_begin; kt < kt_end; ++kt) {
+    const int cur = (kt - kt_begin) & 1;
+    const bool more = kt + 1 < kt_end;
     if (more) load_tiles((kt + 1) * BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
@@ -171,6 +185,50 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     }
     if (more) store_tiles(cur ^ 1);
     __syncthreads();
+  }
+
+  if (split) {
+    // Park this part's partial tile; the last part to finish sums all parts
+    // in part order (so the result does not depend on which finishes last)
+    // and writes C.
+    const int64_t slot = (int64_t)(tile - split_first) * split_parts;
+    float *mine = work + (slot + part) * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int rl = row_base + (i / 4) * G::LM * 4 + (i % 4);
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const int cl = col_base + h * G::LN * 4;
+        *reinterpret_cast<float4 *>(mine + rl * BN + cl) =
+            make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int last;
+    if (threadIdx.x == 0)
+      last = atomicAdd(&counters[tile - split_first], 1u) == (unsigned)(split_parts - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const float *parts0 = work + slot * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int rl = row_base + (i / 4) * G::LM * 4 + (i % 4);
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const int cl = col_base + h * G::LN * 4;
+        float4 sum = __ldcg(reinterpret_cast<const float4 *>(parts0 + rl * BN + cl));
+        for (int p = 1; p < split_parts; ++p) {
+          const float4 v =
+              __ldcg(reinterpret_cast<const float4 *>(parts0 + p * (BM * BN) + rl * BN + cl));
+          sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
+        }
+        acc[i][h * 4] = sum.x, acc[i][h * 4 + 1] = sum.y;
+        acc[i][h * 4 + 2] = sum.z, acc[i][h * 4 + 3] = sum.w;
+      }
+    }
+    if (threadIdx.x == 0) counters[tile - split_first] = 0u;
   }
 
   // ---- epilogue: masked stores, 128-bit where C rows are 16-byte aligned
@@ -197,9 +255,9 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
 template <class G>
 cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, const float *B,
                             int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
-                            cudaStream_t stream) {
+                            int num_sms, cudaStream_t stream) {
   const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
-  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+  if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   auto kern = ab_vec ? sgemm_simt_kernel<G, true> : sgemm_simt_kernel<G, false>;
   if (G::SMEM_BYTES > 48 * 1024) {
     // opt in to more than 48 KB of dynamic shared memory (per device, once)
@@ -213,9 +271,39 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
       if (dev >= 0 && dev < 64) done[ab_vec][dev] = true;
     }
   }
-  kern<<<(unsigned)tiles, G::THREADS, G::SMEM_BYTES, stream>>>(M, N, K, A, lda, B, ldb, C, ldc,
-                                                               c_vec);
-  return cudaGetLastError();
+  // Tail split: when the tiles leave a last wave that is at most half full,
+  // its tiles are split along K so that the wave's blocks finish sooner.
+  const int64_t slots = (int64_t)num_sms * G::MIN_BLOCKS;
+  const int64_t rem = tiles % slots;
+  const int KT = (K + G::BK - 1) / G::BK;
+  int parts = 1;
+  if (rem > 0 && num_sms > 0) parts = (int)(slots / rem < 8 ? slots / rem : 8);
+  while (parts > 1 && KT < 4 * parts) --parts;  // keep at least 4 k-blocks per part
+  int64_t split_first = tiles, grid = tiles;
+  float *work = nullptr;
+  unsigned int *counters = nullptr;
+  void *scratch = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (parts > 1) {
+    split_first = tiles - rem;
+    grid = split_first + rem * parts;
+    const size_t work_bytes = (size_t)(rem * parts) * G::BM * G::BN * sizeof(float);
+    e = cudaMallocAsync(&scratch, work_bytes + (size_t)rem * sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    work = static_cast<float *>(scratch);
+    counters = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + work_bytes);
+    e = cudaMemsetAsync(counters, 0, (size_t)rem * sizeof(unsigned int), stream);
+  }
+  if (e == cudaSuccess) {
+    kern<<<(unsigned)grid, G::THREADS, G::SMEM_BYTES, stream>>>(
+        M, N, K, A, lda, B, ldb, C, ldc, c_vec, (int)split_first, parts, work, counters);
+    e = cudaGetLastError();
+  }
+  if (scratch) {
+    const cudaError_t e2 = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
 }
 
 __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ldc) {
@@ -233,10 +321,10 @@ __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ld
 using SimtShipped = SimtCfg<128, 256, 16, 2, 4, 8, 1>;
 
 cudaError_t launch_simt(int M, int N, int K, const float *A, int64_t lda, const float *B,
-                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
+                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec, int num_sms,
                         cudaStream_t stream) {
-  const cudaError_t e =
-      launch_simt_cfg<SimtShipped>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, stream);
+  const cudaError_t e = launch_simt_cfg<SimtShipped>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
+                                                     c_vec, num_sms, stream);
   if (e == cudaSuccess) count_launch();
   return e;
 }

@@ -153,3 +153,19 @@ def test_streams_are_honoured():
     ref, S = gu.oracle_full(A, B)
     gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL["tf32"], "tf32 on side stream")
     gu.assert_close(C2.cpu().numpy(), ref, S, gu.TOL["simt"], "simt on side stream")
+
+
+def test_simt_tail_split_around_wave_boundaries():
+    """The SIMT path splits the tiles of a partial last wave along K and sums
+    the parts in a fixed order.  Tile counts at, just above and two waves
+    above one full wave of the GPU's SMs (tiles of 128 x 256)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for (rows, K) in [(sms, 777), (sms + 8, 1000), (2 * sms + 3, 520), (5, 4096)]:
+        M, N = 128 * rows, 256
+        A, B = inputs.make_random(M, N, K, seed=rows + K, dist="normal")
+        Ad, Bd = A.cuda(), B.cuda()
+        C1 = gu.run("simt", Ad, Bd).clone()
+        C2 = gu.run("simt", Ad, Bd)
+        assert torch.equal(C1, C2), "split sums must not depend on which part finishes last"
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(C2.cpu().numpy(), ref, S, gu.TOL["simt"], f"simt tail {M}x{N}x{K}")
