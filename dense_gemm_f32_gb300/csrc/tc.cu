@@ -26,6 +26,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -448,7 +449,12 @@ struct Cfg2 {
   static constexpr int THREADS = 32 * (2 + kEpiWarps + kSplitWarps);
   // full, empty, ready (3xTF32), accf[2], acce[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;
+  // epilogue staging: per epilogue warp two 32 x 32 fp32 chunks (TMA stores)
+  static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;
+  static constexpr int EPI_BYTES = kEpiWarps * 2 * EPI_CHUNK_BYTES;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
   static constexpr uint32_t B_LAYOUT = kBF16 ? 2u : 1u;
   static constexpr uint32_t B_SBO = kBF16 ? 1024u : 512u;
   static constexpr uint32_t IDESC = (1u << 4) | ((kBF16 ? 1u : 2u) << 7) |
@@ -472,22 +478,24 @@ enum : int {
 template <TcKind KIND>
 __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
-                    int N, int K, int64_t ldc, int c_vec, int group_m) {
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_c, float *__restrict__ C, int M,
+                    int N, int K, int64_t ldc, int c_tma, int group_m) {
   using G = Cfg2<KIND>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_base);
 
-  const uint32_t bars = base + G::STAGES * G::STAGE_BYTES;
+  const uint32_t epi_base = base + G::STAGES * G::STAGE_BYTES;
+  const uint32_t bars = epi_base + G::EPI_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (G::STAGES + s); };
   auto ready_bar = [&](int s) { return bars + 8u * (2 * G::STAGES + s); };
   auto accf_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
-  uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::NUM_BARS * 8;
+  uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::EPI_BYTES + G::NUM_BARS * 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
   auto a_tile = [&](int s) { return base + (uint32_t)(s * G::STAGE_BYTES); };
@@ -521,6 +529,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
+    if (c_tma) tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(tmem_slot)), G::TMEM_COLS);
@@ -664,6 +673,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
   } else if (warp < 2 + G::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    int epi_chunk = 0;  // TMA-store chunks issued by this warp
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
     int acc = 0;
@@ -675,7 +685,8 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
       if (!ok && lane == 0 && !*abort_flag) watchdog_trip(kSite2EpiAccFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int row = tm * G::BM + (int)rank * G::HM + quarter * 32 + lane;
+      const int row0 = tm * G::BM + (int)rank * G::HM + quarter * 32;
+      const int row = row0 + lane;
       float *crow = C + (int64_t)row * ldc;
       const uint32_t t_row =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * G::BN);
@@ -685,18 +696,40 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
         tmem_wait_ld();
         const int col = tn * G::BN + c0;
-        if (row < M) {
-          if (c_vec && col + 32 <= N) {
+        if (c_tma && col + 32 <= N) {
+          // Stage the warp's 32 x 32 chunk (row = lane) in 128B-swizzled shared
+          // memory and write it with one TMA store (full lines; rows past M are
+          // dropped by the hardware).  Only chunks wholly inside N go this way:
+          // at the inner edge a TMA store writes whole 16-byte granules, which
+          // would touch the ldc gap when N is not a multiple of 4.  Two buffers
+          // per warp; before one is refilled, the store issued from it two
+          // chunks ago must have read it.
+          const uint32_t buf = epi_base + (uint32_t)(((warp - 2) * 2 + (epi_chunk & 1)) *
+                                                     G::EPI_CHUNK_BYTES);
+          if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
+          __syncwarp();
+          const uint32_t row_addr = buf + (uint32_t)(lane * 128);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4 *>(crow + col + j) =
-                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col + j < N) crow[col + j] = __uint_as_float(r[j]);
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t dst = row_addr + (uint32_t)(((c ^ (lane & 7)) << 4));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[4 * c]),
+                         "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
+                         : "memory");
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // A box wholly outside C is not issued; a (possibly empty) group
+            // is committed for every chunk so that "at most one group still
+            // reading" always refers to the other buffer.
+            if (row0 < M) tma_store_2d(&tmap_c, buf, col, row0);
+            bulk_commit_group();
+          }
+          ++epi_chunk;
+        } else if (row < M) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col + j < N) crow[col + j] = __uint_as_float(r[j]);
         }
       }
       tc_fence_before();
@@ -707,6 +740,8 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // every TMA store of this warp complete
+    __syncwarp();
   } else if constexpr (G::kSplit) {
     // ------------------------------------- 3xTF32 split warps (both CTAs)
     // Split this CTA's staged tiles into hi (in place) and lo, then release
@@ -841,10 +876,14 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
       G::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const CUtensorMapSwizzle b_swz =
       G::kBF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, G::HM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK, b_swz)) return cudaErrorInvalidValue;
+  // C through TMA stores when its rows start on 16-byte boundaries.
+  memset(&tc, 0, sizeof(tc));
+  const bool c_tma = c_vec && make_map(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32,
+                                       32, CU_TENSOR_MAP_SWIZZLE_128B);
   auto kern = tc2_gemm_kernel<KIND>;
   static int max_clusters[64] = {};
   int dev = 0;
@@ -875,7 +914,8 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   cfg.gridDim = dim3(2 * clusters);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m(16));
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, C, M, N, K, ldc, c_tma ? 1 : 0,
+                         raster_group_m(16));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
