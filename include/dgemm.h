@@ -106,10 +106,10 @@ int gemm_f32_simt(int M, int N, int K,
  * staged by TMA into swizzled shared memory, accumulated in tensor memory.
  * mode = DGEMM_TC_TF32:   each operand is read at TF32 precision; accuracy
  *                         |C - C_exact| <= 2e-3 * (|A| x |B|).
- * mode = DGEMM_TC_3XTF32: each operand is split a = hi + lo (hi = a with the
- *                         low 13 mantissa bits cleared, lo = a - hi, both
- *                         exact TF32 values) and C = A_hi B_hi + A_hi B_lo +
- *                         A_lo B_hi; accuracy <= 1e-5 * (|A| x |B|).
+ * mode = DGEMM_TC_3XTF32: each operand is split a ~ hi + lo (hi = a with the
+ *                         low 13 mantissa bits cleared, lo = a - hi rounded
+ *                         to TF32) and C = A_hi B_hi + A_hi B_lo + A_lo B_hi;
+ *                         accuracy <= 1e-5 * (|A| x |B|).
  * Argument layout as gemm_f32_simt.  Unknown mode: DGEMM_ERR_UNSUPPORTED.
  */
 int gemm_f32_tc(int mode, int M, int N, int K,
