@@ -47,7 +47,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--mode", choices=["tf32", "3xtf32", "simt", "bf16"], default="tf32")
+    p.add_argument("--mode", choices=["tf32", "3xtf32", "simt", "bf16", "fp16"], default="tf32")
     p.add_argument("--no-modes", action="store_true", help="headline only, skip the per-mode table")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -68,10 +68,13 @@ def workload_for(mode, transformer=False, shape=None):
 
     if shape:
         M, N, K = (int(x) for x in shape.split(","))
-        return inputs.Workload(f"uniform {M}x{N}x{K}", M, N, K, 3, "uniform", bf16=(mode == "bf16"))
+        return inputs.Workload(f"uniform {M}x{N}x{K}", M, N, K, 3, "uniform", bf16=(mode == "bf16"),
+                               fp16=(mode == "fp16"))
 
     if mode == "bf16":
         return inputs.TRANSFORMER_BF16
+    if mode == "fp16":
+        return inputs.TRANSFORMER_F16
     return inputs.TRANSFORMER_F32 if transformer else inputs.SQUARE_8192
 
 
@@ -94,6 +97,8 @@ def mode_peak(mode, peaks, num_sms):
     bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     if mode == "bf16":
         return "tensor", bf16, "measured cuBLAS bf16 burst"
+    if mode == "fp16":
+        return "tensor", bf16, "measured cuBLAS bf16 burst (fp16 and bf16 share the nominal rate)"
     r = NOMINAL_PF["tf32"] / NOMINAL_PF["bf16"]
     return "tensor", bf16 * r, f"measured bf16 burst x nominal tf32/bf16 ratio {r:.4f}"
 
@@ -323,6 +328,8 @@ def device_inputs(w, mode, device):
     A, B = inputs.make(w)
     if mode == "bf16" and not w.bf16:
         A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    if mode == "fp16" and not w.fp16:
+        A, B = A.to(torch.float16), B.to(torch.float16)
     return A, B, A.to(device), B.to(device)
 
 
@@ -463,7 +470,7 @@ def run_ours(args, dist):
     modes = {}
     if not args.no_modes:
         table = [("simt", False), ("tf32", False), ("3xtf32", False), ("bf16", True),
-                 ("tf32", True)]
+                 ("fp16", True), ("tf32", True)]
         for m, tr in table:
             wm = workload_for(m, transformer=tr)
             if m == mode and wm.name == w.name:
@@ -497,7 +504,8 @@ def run_ours(args, dist):
             "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": agg["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"tf32": "tf32", "3xtf32": "3xtf32", "simt": "f32", "bf16": "bf16"}[mode],
+            "dtype": {"tf32": "tf32", "3xtf32": "3xtf32", "simt": "f32", "bf16": "bf16",
+                      "fp16": "fp16"}[mode],
             "data": "synthetic (seeded, shapes and distributions of the workload)",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "mode": mode,
                        "layout": "row-major, compact leading dimensions",

@@ -14,10 +14,11 @@ from ._lib import (  # noqa: F401  (re-exported C entry points)
     ERR_NULL_POINTER, ERR_SCRATCH_LIMIT, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, LIB_PATH,
     NOALLOC_SCRATCH_BYTES, OK, TC_3XTF32,
     TC_TF32, LibraryMissing, dgemm_kernel_launches, dgemm_last_cuda_error, dgemm_status_string, dgemm_version,
-    dgemm_watchdog_status, gemm_bf16_tc, gemm_f32_simt, gemm_f32_tc, gemm_f32_tc_noalloc, load,
+    dgemm_watchdog_status, gemm_bf16_tc, gemm_f16_tc, gemm_f32_simt, gemm_f32_tc,
+    gemm_f32_tc_noalloc, load,
 )
 
-MODES = ("simt", "tf32", "3xtf32", "bf16")
+MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16")
 
 
 class DgemmError(RuntimeError):
@@ -50,7 +51,8 @@ def matmul(A, B, mode="tf32", out=None, stream=None):
     """C = A @ B on the GPU through the C ABI.
 
     A: (M, K), B: (K, N) CUDA tensors, float32 for modes simt / tf32 / 3xtf32,
-    bfloat16 for mode bf16; rows may be strided (leading dimension = stride(0)).
+    bfloat16 for mode bf16, float16 for mode fp16; rows may be strided
+    (leading dimension = stride(0)).
     out: optional float32 (M, N) CUDA tensor view to overwrite.
     stream: a torch.cuda.Stream or raw handle; default the current stream.
     """
@@ -58,7 +60,7 @@ def matmul(A, B, mode="tf32", out=None, stream=None):
 
     if mode not in MODES:
         raise ValueError(f"mode must be one of {MODES}")
-    want = torch.bfloat16 if mode == "bf16" else torch.float32
+    want = {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
     if A.dtype != want or B.dtype != want:
         raise TypeError(f"mode {mode} takes {want} inputs, got {A.dtype} and {B.dtype}")
     M, K = A.shape
@@ -81,7 +83,9 @@ def matmul(A, B, mode="tf32", out=None, stream=None):
         st = gemm_f32_tc(TC_TF32, M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
     elif mode == "3xtf32":
         st = gemm_f32_tc(TC_3XTF32, M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
-    else:
+    elif mode == "bf16":
         st = gemm_bf16_tc(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    else:
+        st = gemm_f16_tc(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
     check(st, f"gemm ({mode})")
     return out

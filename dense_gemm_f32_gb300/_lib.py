@@ -29,7 +29,7 @@ TC_3XTF32 = 1
 
 EXPORTED = ("gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
             "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-            "dgemm_kernel_launches", "gemm_f32_tc_noalloc")
+            "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc")
 
 _lib = None
 
@@ -69,6 +69,8 @@ def load():
     lib.dgemm_kernel_launches.restype = ctypes.c_ulonglong
     lib.gemm_f32_tc_noalloc.argtypes = [i] + gemm_args
     lib.gemm_f32_tc_noalloc.restype = i
+    lib.gemm_f16_tc.argtypes = gemm_args
+    lib.gemm_f16_tc.restype = i
     _lib = lib
     return lib
 
@@ -89,6 +91,10 @@ def gemm_f32_tc_noalloc(mode, M, N, K, A, lda, B, ldb, C, ldc, stream=0):
 
 def gemm_bf16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
     return load().gemm_bf16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
+    return load().gemm_f16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def dgemm_status_string(status):

@@ -21,7 +21,7 @@ UNITS = ["api.cu", "simt.cu", "tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 EXPORTS = ["gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
            "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-           "dgemm_kernel_launches", "gemm_f32_tc_noalloc"]
+           "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc"]
 
 
 def _nvcc():

@@ -139,7 +139,7 @@ inline bool tma_ok(const void *p, int64_t ld, int es) { return aligned(p, 16) &&
 // their rows do not start on 16-byte boundaries.
 int run_tc(dg::TcKind kind, int M, int N, int K, const void *A, int lda, const void *B, int ldb,
            float *C, int ldc, int num_sms, cudaStream_t stream) {
-  const int es = (kind == dg::TcKind::kBF16) ? 2 : 4;
+  const int es = (kind == dg::TcKind::kBF16 || kind == dg::TcKind::kF16) ? 2 : 4;
   const int64_t pitch_elems = 16 / es;
   const void *Ause = A, *Buse = B;
   int64_t lda_use = lda, ldb_use = ldb;
@@ -288,6 +288,16 @@ int gemm_bf16_tc(int M, int N, int K, const unsigned short *A, int lda, const un
   if (st != DGEMM_OK || none) return st;
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
   return run_tc(dg::TcKind::kBF16, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
+}
+
+int gemm_f16_tc(int M, int N, int K, const unsigned short *A, int lda, const unsigned short *B,
+                int ldb, float *C, int ldc, cudaStream_t stream) {
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 2, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  return run_tc(dg::TcKind::kF16, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
 }
 
 const char *dgemm_status_string(int status) {

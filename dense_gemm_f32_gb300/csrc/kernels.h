@@ -20,7 +20,7 @@ cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
                              cudaStream_t stream);
 
 // Element type of a tensor-core GEMM's operands.
-enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2 };
+enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2, kF16 = 3 };
 
 // tcgen05 GEMM.  A (M x K) and B (K x N) row-major with leading dimensions in
 // elements; both must satisfy the TMA rules (16-byte aligned base, leading

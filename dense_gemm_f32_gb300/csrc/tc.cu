@@ -56,10 +56,13 @@ enum : int {
 
 template <TcKind KIND, int BN_>
 struct Cfg {
-  static constexpr bool kBF16 = KIND == TcKind::kBF16;
+  // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
+  static constexpr bool k16 = KIND == TcKind::kBF16 || KIND == TcKind::kF16;
+  // operand format code of the instruction descriptor: F16 0, BF16 1, TF32 2
+  static constexpr uint32_t kFmt = KIND == TcKind::kF16 ? 0u : KIND == TcKind::kBF16 ? 1u : 2u;
   static constexpr bool kSplit = KIND == TcKind::k3xTF32;
   static constexpr int BN = BN_;
-  static constexpr int ES = kBF16 ? 2 : 4;        // operand element bytes
+  static constexpr int ES = k16 ? 2 : 4;        // operand element bytes
   static constexpr int BK = 128 / ES;             // k per stage: one 128-B swizzle row
   static constexpr int UMMA_K = 32 / ES;          // k per MMA instruction (32 bytes)
   static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per stage (per product)
@@ -93,13 +96,13 @@ struct Cfg {
   // type 1, TMA mode SWIZZLE_128B_ATOM_32B).  Rows of a B box are contiguous
   // 128-byte lines, so the K-group stride is (group rows) x 128 B: 512 B
   // covers both a 4-row and an 8-row swizzle period for the 8-row MMA slice.
-  static constexpr uint32_t B_LAYOUT = kBF16 ? 2u : 1u;
-  static constexpr uint32_t B_SBO = kBF16 ? 1024u : 512u;
+  static constexpr uint32_t B_LAYOUT = k16 ? 2u : 1u;
+  static constexpr uint32_t B_SBO = k16 ? 1024u : 512u;
 
   // Instruction descriptor: D fp32, A/B TF32 or BF16, A K-major, B MN-major,
   // N >> 3 at bit 17, M >> 4 at bit 24.
-  static constexpr uint32_t IDESC = (1u << 4) | ((kBF16 ? 1u : 2u) << 7) |
-                                    ((kBF16 ? 1u : 2u) << 10) | (0u << 15) | (1u << 16) |
+  static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) |
+                                    (kFmt << 10) | (0u << 15) | (1u << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 };
 
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
               umma_tf32(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32(d_tmem, ad, bdl, G::IDESC, 1u);      // A_hi B_lo
               umma_tf32(d_tmem, ad, bd, G::IDESC, 1u);       // A_hi B_hi
-            } else if constexpr (G::kBF16) {
+            } else if constexpr (G::k16) {
               umma_f16(d_tmem, ad, bd, G::IDESC, accum);
             } else {
               umma_tf32(d_tmem, ad, bd, G::IDESC, accum);
@@ -424,11 +427,14 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
 //    its way, then both CTAs meet at a cluster barrier and free TMEM.
 template <TcKind KIND>
 struct Cfg2 {
-  static constexpr bool kBF16 = KIND == TcKind::kBF16;
+  // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
+  static constexpr bool k16 = KIND == TcKind::kBF16 || KIND == TcKind::kF16;
+  // operand format code of the instruction descriptor: F16 0, BF16 1, TF32 2
+  static constexpr uint32_t kFmt = KIND == TcKind::kF16 ? 0u : KIND == TcKind::kBF16 ? 1u : 2u;
   static constexpr bool kSplit = KIND == TcKind::k3xTF32;
   static constexpr int BM = 256, BN = 256;           // pair tile
   static constexpr int HM = 128, HN = 128;           // per-CTA halves
-  static constexpr int ES = kBF16 ? 2 : 4;
+  static constexpr int ES = k16 ? 2 : 4;
   static constexpr int BK = 128 / ES;
   static constexpr int UMMA_K = 32 / ES;
   static constexpr int KSTEPS = BK / UMMA_K;
@@ -452,10 +458,10 @@ struct Cfg2 {
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
-  static constexpr uint32_t B_LAYOUT = kBF16 ? 2u : 1u;
-  static constexpr uint32_t B_SBO = kBF16 ? 1024u : 512u;
-  static constexpr uint32_t IDESC = (1u << 4) | ((kBF16 ? 1u : 2u) << 7) |
-                                    ((kBF16 ? 1u : 2u) << 10) | (0u << 15) | (1u << 16) |
+  static constexpr uint32_t B_LAYOUT = k16 ? 2u : 1u;
+  static constexpr uint32_t B_SBO = k16 ? 1024u : 512u;
+  static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) |
+                                    (kFmt << 10) | (0u << 15) | (1u << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(kSplitWarp0 == 2 + kEpiWarps, "split warps follow the epilogue warps");
@@ -633,7 +639,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
               umma_tf32_pair(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32_pair(d_tmem, ad, bdl, G::IDESC, 1u);     // A_hi B_lo
               umma_tf32_pair(d_tmem, ad, bd, G::IDESC, 1u);      // A_hi B_hi
-            } else if constexpr (G::kBF16) {
+            } else if constexpr (G::k16) {
               umma_f16_pair(d_tmem, ad, bd, G::IDESC, accum);
             } else {
               umma_tf32_pair(d_tmem, ad, bd, G::IDESC, accum);
@@ -842,10 +848,12 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
                        cudaStream_t stream) {
   using G = Cfg<KIND, BN>;
   const CUtensorMapDataType dt =
-      G::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+      KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+      : KIND == TcKind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUtensorMap ta, tb;
   const CUtensorMapSwizzle b_swz =
-      G::kBF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+      G::k16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
   if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK, b_swz)) return cudaErrorInvalidValue;
@@ -874,9 +882,11 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, cudaStream_t stream) {
   using G = Cfg2<KIND>;
   const CUtensorMapDataType dt =
-      G::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+      KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+      : KIND == TcKind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const CUtensorMapSwizzle b_swz =
-      G::kBF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+      G::k16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
   CUtensorMap ta, tb, tc;
   if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, G::HM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -980,6 +990,11 @@ cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t l
         return launch_cfg2<TcKind::kBF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
       return launch_cfg<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                             stream);
+    case TcKind::kF16:
+      if (use_pair(M, N, num_sms))
+        return launch_cfg2<TcKind::kF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
+      return launch_cfg<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                           stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -176,6 +176,26 @@ int gemm_f32_tc_noalloc(int mode, int M, int N, int K,
 /* Size in bytes of the fixed scratch array gemm_f32_tc_noalloc uses. */
 #define DGEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
+/*
+ * gemm_f16_tc -- FP16 inputs, FP32 accumulate, FP32 output, on tcgen05.
+ *
+ * The tensor-core input type of "SGEMM 优化旅程" Level 6 (half operands with
+ * a float accumulator, there through WMMA fragments) and the first entry of
+ * Lesson 8 section 二十二's list of tensor-core formats; the same kernels as
+ * gemm_bf16_tc with IEEE binary16 operands.
+ * A: M x K float16 (raw 16-bit patterns), row-major, lda >= max(1, K).
+ * B: K x N float16, row-major, ldb >= max(1, N).
+ * C: M x N fp32, row-major, ldc >= max(1, N); overwritten.
+ * The fp16 inputs are exact, so only the FP32 accumulation rounds: at most
+ * K/16 rounded additions of the accumulator, |C - C_exact| <= 2e-4 *
+ * (|A| x |B|) for K <= 16384.
+ */
+int gemm_f16_tc(int M, int N, int K,
+                const unsigned short *A, int lda,
+                const unsigned short *B, int ldb,
+                float *C, int ldc,
+                cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *dgemm_status_string(int status);
 

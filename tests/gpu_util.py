@@ -5,13 +5,16 @@ import torch
 import oracle
 
 # |C - C_exact| <= tol * S elementwise, S = |A| x |B|; one tolerance per mode.
-TOL = {"simt": 1e-5, "3xtf32": 1e-5, "tf32": 2e-3, "bf16": 8e-3}
+# fp16: the inputs are exact, only the fp32 accumulation rounds (at most K/16
+# rounded accumulator additions of 2^-23 each: 1.2e-4 at K = 16384).
+TOL = {"simt": 1e-5, "3xtf32": 1e-5, "tf32": 2e-3, "bf16": 8e-3, "fp16": 2e-4}
 FP32_MODES = ("simt", "tf32", "3xtf32")
-ALL_MODES = ("simt", "tf32", "3xtf32", "bf16")
+HALF_MODES = ("bf16", "fp16")
+ALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16")
 
 
 def in_dtype(mode):
-    return torch.bfloat16 if mode == "bf16" else torch.float32
+    return {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
 
 
 def np_inputs(A, B):

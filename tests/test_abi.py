@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
 P = 0x10000  # a fake, 16-byte aligned address: never dereferenced by these calls
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
 def test_invalid_sizes_rejected(lib, fn):
     call = _caller(fn)
     E = dg.ERR_INVALID_VALUE
@@ -61,7 +61,7 @@ def test_invalid_sizes_rejected(lib, fn):
     assert call(4, 4, 0, P, 0, P * 2, 4, P * 3, 4) == E     # lda must be >= 1
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
 def test_empty_output_is_a_no_op(lib, fn):
     call = _caller(fn)
     # nothing to do: pointers are not looked at, no CUDA call is made
@@ -69,7 +69,7 @@ def test_empty_output_is_a_no_op(lib, fn):
     assert call(5, 0, 5, 0, 5, 0, 1, 0, 1) == dg.OK
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
 def test_null_pointers_rejected(lib, fn):
     call = _caller(fn)
     E = dg.ERR_NULL_POINTER
@@ -79,10 +79,10 @@ def test_null_pointers_rejected(lib, fn):
     assert call(4, 4, 0, P, 1, P * 2, 4, 0, 4) == E       # K == 0 still writes C
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
 def test_misaligned_pointers_rejected(lib, fn):
     call = _caller(fn)
-    es = 2 if fn == "bf16" else 4
+    es = 2 if fn in ("bf16", "fp16") else 4
     E = dg.ERR_MISALIGNED
     assert call(4, 4, 4, P + 1, 4, P * 2, 4, P * 4, 4) == E
     assert call(4, 4, 4, P, 4, P * 2 + 1, 4, P * 4, 4) == E
@@ -91,10 +91,10 @@ def test_misaligned_pointers_rejected(lib, fn):
         assert call(4, 4, 4, P + 2, 4, P * 2, 4, P * 4, 4) == E
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
 def test_alias_rejected(lib, fn):
     call = _caller(fn)
-    es = 2 if fn == "bf16" else 4
+    es = 2 if fn in ("bf16", "fp16") else 4
     E = dg.ERR_ALIAS
     # C starts inside A's span / B's span
     assert call(8, 8, 8, P, 8, P * 4, 8, P + 8 * 8 * es - 4, 8) == E
@@ -132,4 +132,6 @@ def _caller(fn):
         return lambda *a: dg.gemm_f32_tc(dg.TC_TF32, *a, 0)
     if fn == "3xtf32":
         return lambda *a: dg.gemm_f32_tc(dg.TC_3XTF32, *a, 0)
+    if fn == "fp16":
+        return lambda *a: dg.gemm_f16_tc(*a, 0)
     return lambda *a: dg.gemm_bf16_tc(*a, 0)

@@ -30,8 +30,8 @@ def _built():
 
 def _full_case(w, mode):
     A, B = inputs.make(w)
-    if mode == "bf16" and not w.bf16:
-        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    if mode in gu.HALF_MODES and A.dtype != gu.in_dtype(mode):
+        A, B = A.float().to(gu.in_dtype(mode)), B.float().to(gu.in_dtype(mode))
     C = gu.run(mode, A.cuda(), B.cuda())
     ref, S = gu.oracle_full(A, B)
     gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL[mode], f"{w.name} {mode}")
@@ -80,8 +80,8 @@ def test_ragged_1000x1013x997(mode):
 
 def _sampled(w, mode, nrows=48):
     A, B = inputs.make(w)
-    if mode == "bf16" and not w.bf16:
-        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+    if mode in gu.HALF_MODES and A.dtype != gu.in_dtype(mode):
+        A, B = A.float().to(gu.in_dtype(mode)), B.float().to(gu.in_dtype(mode))
     C = gu.run(mode, A.cuda(), B.cuda())
     g = np.random.default_rng(w.seed)
     rows = np.unique(np.concatenate([[0, 127, 128, w.M - 1],
@@ -103,3 +103,8 @@ def test_transformer_bf16_sampled_rows():
 
 def test_transformer_tf32_sampled_rows():
     _sampled(inputs.TRANSFORMER_F32, "tf32", nrows=24)
+
+
+def test_transformer_fp16_sampled_rows():
+    """The transformer-layer draws rounded to fp16 instead of bf16."""
+    _sampled(inputs.TRANSFORMER_F16, "fp16", nrows=24)
