@@ -12,7 +12,8 @@ libdgemm.so every call raises.
 from ._lib import (  # noqa: F401  (re-exported C entry points)
     ERR_ALIAS, ERR_ARCH, ERR_CUDA, ERR_INVALID_POINTER, ERR_INVALID_VALUE, ERR_MISALIGNED,
     ERR_NULL_POINTER, ERR_SCRATCH_LIMIT, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, LIB_PATH,
-    NOALLOC_SCRATCH_BYTES, OK, TC_3XTF32,
+    NOALLOC_SCRATCH_BYTES, OK, OP_N, OP_T, PATH_3XTF32, PATH_BF16, PATH_FP16, PATH_SIMT,
+    PATH_TF32, TC_3XTF32, dgemm_gemm_ex,
     TC_TF32, LibraryMissing, dgemm_kernel_launches, dgemm_last_cuda_error, dgemm_status_string, dgemm_version,
     dgemm_watchdog_status, gemm_bf16_tc, gemm_f16_tc, gemm_f32_simt, gemm_f32_tc,
     gemm_f32_tc_noalloc, load,
@@ -47,12 +48,17 @@ def _ld(X, cols):
     return X.stride(0)
 
 
-def matmul(A, B, mode="tf32", out=None, stream=None):
-    """C = A @ B on the GPU through the C ABI.
+_PATH = {"simt": PATH_SIMT, "tf32": PATH_TF32, "3xtf32": PATH_3XTF32, "bf16": PATH_BF16,
+         "fp16": PATH_FP16}
 
-    A: (M, K), B: (K, N) CUDA tensors, float32 for modes simt / tf32 / 3xtf32,
+
+def matmul(A, B, mode="tf32", out=None, stream=None, trans_a=False, trans_b=False):
+    """C = op(A) @ op(B) on the GPU through the C ABI.
+
+    A, B: CUDA tensors as stored, float32 for modes simt / tf32 / 3xtf32,
     bfloat16 for mode bf16, float16 for mode fp16; rows may be strided
-    (leading dimension = stride(0)).
+    (leading dimension = stride(0)).  op(A) = A.T when trans_a (A stored
+    K x M), else A (M x K); op(B) = B.T when trans_b (B stored N x K), else B.
     out: optional float32 (M, N) CUDA tensor view to overwrite.
     stream: a torch.cuda.Stream or raw handle; default the current stream.
     """
@@ -63,10 +69,12 @@ def matmul(A, B, mode="tf32", out=None, stream=None):
     want = {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
     if A.dtype != want or B.dtype != want:
         raise TypeError(f"mode {mode} takes {want} inputs, got {A.dtype} and {B.dtype}")
-    M, K = A.shape
-    K2, N = B.shape
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("expected 2-D matrices")
+    M, K = (A.shape[1], A.shape[0]) if trans_a else (A.shape[0], A.shape[1])
+    K2, N = (B.shape[1], B.shape[0]) if trans_b else (B.shape[0], B.shape[1])
     if K != K2:
-        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+        raise ValueError(f"inner dimensions differ: op(A) is {M}x{K}, op(B) is {K2}x{N}")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     elif out.dtype != torch.float32 or tuple(out.shape) != (M, N):
@@ -75,9 +83,12 @@ def matmul(A, B, mode="tf32", out=None, stream=None):
         stream = torch.cuda.current_stream(A.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    lda, ldb, ldc = _ld(A, K), _ld(B, N), _ld(out, N)
+    lda, ldb, ldc = _ld(A, A.shape[1]), _ld(B, B.shape[1]), _ld(out, N)
     pa, pb, pc = A.data_ptr(), B.data_ptr(), out.data_ptr()
-    if mode == "simt":
+    if trans_a or trans_b:
+        st = dgemm_gemm_ex(_PATH[mode], OP_T if trans_a else OP_N, OP_T if trans_b else OP_N,
+                           M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    elif mode == "simt":
         st = gemm_f32_simt(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
     elif mode == "tf32":
         st = gemm_f32_tc(TC_TF32, M, N, K, pa, lda, pb, ldb, pc, ldc, stream)

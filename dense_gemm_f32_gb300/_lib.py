@@ -27,9 +27,13 @@ NOALLOC_SCRATCH_BYTES = 16 << 20
 TC_TF32 = 0
 TC_3XTF32 = 1
 
+OP_N = 0
+OP_T = 1
+PATH_SIMT, PATH_TF32, PATH_3XTF32, PATH_BF16, PATH_FP16 = range(5)
+
 EXPORTED = ("gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
             "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-            "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc")
+            "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc", "dgemm_gemm_ex")
 
 _lib = None
 
@@ -71,6 +75,8 @@ def load():
     lib.gemm_f32_tc_noalloc.restype = i
     lib.gemm_f16_tc.argtypes = gemm_args
     lib.gemm_f16_tc.restype = i
+    lib.dgemm_gemm_ex.argtypes = [i, i, i] + gemm_args
+    lib.dgemm_gemm_ex.restype = i
     _lib = lib
     return lib
 
@@ -95,6 +101,10 @@ def gemm_bf16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
 
 def gemm_f16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
     return load().gemm_f16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def dgemm_gemm_ex(path, op_a, op_b, M, N, K, A, lda, B, ldb, C, ldc, stream=0):
+    return load().dgemm_gemm_ex(path, op_a, op_b, M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def dgemm_status_string(status):

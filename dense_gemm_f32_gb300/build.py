@@ -17,11 +17,15 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdgemm.so")
 HEADER = os.path.join(ROOT, "include", "dgemm.h")
-UNITS = ["api.cu", "simt.cu", "tc.cu"]
+# (source, object name, defines): simt.cu and tc.cu are compiled once per
+# operand layout so that the four layouts build in parallel.
+UNITS = ([("api.cu", "api", [])]
+         + [("simt.cu", f"simt_{u}", [f"-DDGEMM_SIMT_UNIT={u}"]) for u in range(4)]
+         + [("tc.cu", f"tc_{u}", [f"-DDGEMM_TC_UNIT={u}"]) for u in range(4)])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 EXPORTS = ["gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
            "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-           "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc"]
+           "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc", "dgemm_gemm_ex"]
 
 
 def _nvcc():
@@ -44,15 +48,16 @@ def _stale():
 
 
 def _compile(nvcc, unit):
-    src = os.path.join(CSRC, unit)
-    obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
+    source, name, defines = unit
+    src = os.path.join(CSRC, source)
+    obj = os.path.join(BUILD, name + ".o")
     cmd = [nvcc, *ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC",
-           "-Xptxas", "-v", "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+           "-Xptxas", "-v", *defines, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
-    with open(os.path.join(BUILD, f"ptxas_{unit}.log"), "w") as f:
+    with open(os.path.join(BUILD, f"ptxas_{name}.log"), "w") as f:
         f.write(r.stdout + r.stderr)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on {unit}:\n{r.stderr[-6000:]}")
+        raise RuntimeError(f"nvcc failed on {name}:\n{r.stderr[-6000:]}")
     return obj
 
 
@@ -62,7 +67,7 @@ def build(force=False, verbose=False):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(len(UNITS), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda u: _compile(nvcc, u), UNITS))
     vs = os.path.join(BUILD, "exports.map")
     with open(vs, "w") as f:
@@ -74,8 +79,8 @@ def build(force=False, verbose=False):
         raise RuntimeError(f"link failed:\n{r.stderr[-6000:]}")
     os.replace(tmp, LIB)
     if verbose:
-        for u in UNITS:
-            with open(os.path.join(BUILD, f"ptxas_{u}.log")) as f:
+        for _, name, _ in UNITS:
+            with open(os.path.join(BUILD, f"ptxas_{name}.log")) as f:
                 sys.stdout.write(f.read())
     return LIB
 

@@ -99,11 +99,16 @@ inline Span span(const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t 
 inline bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
 // Steps 2-8 of the check list.  *nothing_to_do is set when M or N is zero.
-int validate(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C,
-             int ldc, int in_bytes, bool *nothing_to_do, int *dev, int *num_sms) {
+// a_t / b_t: A is stored K x M (op(A) = A^T) / B is stored N x K.
+int validate(int M, int N, int K, bool a_t, bool b_t, const void *A, int lda, const void *B,
+             int ldb, const void *C, int ldc, int in_bytes, bool *nothing_to_do, int *dev,
+             int *num_sms) {
   *nothing_to_do = false;
   if (M < 0 || N < 0 || K < 0) return DGEMM_ERR_INVALID_VALUE;
-  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+  const int a_rows = a_t ? K : M, a_cols = a_t ? M : K;
+  const int b_rows = b_t ? N : K, b_cols = b_t ? K : N;
+  if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1) ||
+      ldc < (N > 1 ? N : 1))
     return DGEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) {
     *nothing_to_do = true;
@@ -114,7 +119,8 @@ int validate(int M, int N, int K, const void *A, int lda, const void *B, int ldb
   if (K > 0 && (!aligned(A, in_bytes) || !aligned(B, in_bytes))) return DGEMM_ERR_MISALIGNED;
   if (K > 0) {
     const Span c = span(C, M, N, ldc, 4);
-    if (overlap(c, span(A, M, K, lda, in_bytes)) || overlap(c, span(B, K, N, ldb, in_bytes)))
+    if (overlap(c, span(A, a_rows, a_cols, lda, in_bytes)) ||
+        overlap(c, span(B, b_rows, b_cols, ldb, in_bytes)))
       return DGEMM_ERR_ALIAS;
   }
   int st = current_device(dev, num_sms);
@@ -137,37 +143,39 @@ inline bool tma_ok(const void *p, int64_t ld, int es) { return aligned(p, 16) &&
 
 // Tensor-core GEMM with operands re-pitched into stream-ordered scratch when
 // their rows do not start on 16-byte boundaries.
-int run_tc(dg::TcKind kind, int M, int N, int K, const void *A, int lda, const void *B, int ldb,
-           float *C, int ldc, int num_sms, cudaStream_t stream) {
+int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A, int lda,
+           const void *B, int ldb, float *C, int ldc, int num_sms, cudaStream_t stream) {
   const int es = (kind == dg::TcKind::kBF16 || kind == dg::TcKind::kF16) ? 2 : 4;
   const int64_t pitch_elems = 16 / es;
+  const int a_rows = a_t ? K : M, a_cols = a_t ? M : K;  // storage shapes
+  const int b_rows = b_t ? N : K, b_cols = b_t ? K : N;
   const void *Ause = A, *Buse = B;
   int64_t lda_use = lda, ldb_use = ldb;
   void *scratch = nullptr;
   const bool a_ok = tma_ok(A, lda, es), b_ok = tma_ok(B, ldb, es);
   cudaError_t e = cudaSuccess;
   if (!a_ok || !b_ok) {
-    const int64_t lda2 = (K + pitch_elems - 1) / pitch_elems * pitch_elems;
-    const int64_t ldb2 = (N + pitch_elems - 1) / pitch_elems * pitch_elems;
-    const size_t a_bytes = a_ok ? 0 : (size_t)((int64_t)M * lda2 * es + 255) / 256 * 256;
-    const size_t b_bytes = b_ok ? 0 : (size_t)((int64_t)K * ldb2 * es + 255) / 256 * 256;
+    const int64_t lda2 = (a_cols + pitch_elems - 1) / pitch_elems * pitch_elems;
+    const int64_t ldb2 = (b_cols + pitch_elems - 1) / pitch_elems * pitch_elems;
+    const size_t a_bytes = a_ok ? 0 : (size_t)((int64_t)a_rows * lda2 * es + 255) / 256 * 256;
+    const size_t b_bytes = b_ok ? 0 : (size_t)((int64_t)b_rows * ldb2 * es + 255) / 256 * 256;
     e = cudaMallocAsync(&scratch, a_bytes + b_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (re-pitch scratch)");
     char *s = static_cast<char *>(scratch);
     if (!a_ok) {
-      e = dg::launch_repitch(A, lda, s, lda2, M, K, es, num_sms, stream);
+      e = dg::launch_repitch(A, lda, s, lda2, a_rows, a_cols, es, num_sms, stream);
       if (e != cudaSuccess) goto done;
       Ause = s;
       lda_use = lda2;
     }
     if (!b_ok) {
-      e = dg::launch_repitch(B, ldb, s + a_bytes, ldb2, K, N, es, num_sms, stream);
+      e = dg::launch_repitch(B, ldb, s + a_bytes, ldb2, b_rows, b_cols, es, num_sms, stream);
       if (e != cudaSuccess) goto done;
       Buse = s + a_bytes;
       ldb_use = ldb2;
     }
   }
-  e = dg::launch_tc(kind, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
+  e = dg::launch_tc(kind, a_t, b_t, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
                     aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
 done:
   if (scratch != nullptr) {
@@ -233,7 +241,7 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
       ldb_use = ldb2;
     }
   }
-  e = dg::launch_tc(kind, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
+  e = dg::launch_tc(kind, false, false, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
                     aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
   return after_launch(e, "tensor-core GEMM launch (no-alloc)");
 }
@@ -247,7 +255,7 @@ int gemm_f32_tc_noalloc(int mode, int M, int N, int K, const float *A, int lda, 
   if (mode != DGEMM_TC_TF32 && mode != DGEMM_TC_3XTF32) return DGEMM_ERR_UNSUPPORTED;
   bool none = false;
   int dev = 0, sms = 0;
-  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
+  int st = validate(M, N, K, false, false, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
   if (st != DGEMM_OK || none) return st;
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
   return run_tc_noalloc(mode == DGEMM_TC_TF32 ? dg::TcKind::kTF32 : dg::TcKind::k3xTF32, M, N, K,
@@ -258,13 +266,13 @@ int gemm_f32_simt(int M, int N, int K, const float *A, int lda, const float *B, 
                   float *C, int ldc, cudaStream_t stream) {
   bool none = false;
   int dev = 0, sms = 0;
-  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
+  int st = validate(M, N, K, false, false, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
   if (st != DGEMM_OK || none) return st;
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
   const bool ab_vec = aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0;
   const bool c_vec = aligned(C, 16) && ldc % 4 == 0;
   return after_launch(
-      dg::launch_simt(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, sms, stream),
+      dg::launch_simt(false, false, M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, sms, stream),
       "SIMT GEMM launch");
 }
 
@@ -273,31 +281,58 @@ int gemm_f32_tc(int mode, int M, int N, int K, const float *A, int lda, const fl
   if (mode != DGEMM_TC_TF32 && mode != DGEMM_TC_3XTF32) return DGEMM_ERR_UNSUPPORTED;
   bool none = false;
   int dev = 0, sms = 0;
-  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
+  int st = validate(M, N, K, false, false, A, lda, B, ldb, C, ldc, 4, &none, &dev, &sms);
   if (st != DGEMM_OK || none) return st;
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
-  return run_tc(mode == DGEMM_TC_TF32 ? dg::TcKind::kTF32 : dg::TcKind::k3xTF32, M, N, K, A, lda,
-                B, ldb, C, ldc, sms, stream);
+  return run_tc(mode == DGEMM_TC_TF32 ? dg::TcKind::kTF32 : dg::TcKind::k3xTF32, false, false, M,
+                N, K, A, lda, B, ldb, C, ldc, sms, stream);
 }
 
 int gemm_bf16_tc(int M, int N, int K, const unsigned short *A, int lda, const unsigned short *B,
                  int ldb, float *C, int ldc, cudaStream_t stream) {
   bool none = false;
   int dev = 0, sms = 0;
-  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 2, &none, &dev, &sms);
+  int st = validate(M, N, K, false, false, A, lda, B, ldb, C, ldc, 2, &none, &dev, &sms);
   if (st != DGEMM_OK || none) return st;
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
-  return run_tc(dg::TcKind::kBF16, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
+  return run_tc(dg::TcKind::kBF16, false, false, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
 }
 
 int gemm_f16_tc(int M, int N, int K, const unsigned short *A, int lda, const unsigned short *B,
                 int ldb, float *C, int ldc, cudaStream_t stream) {
   bool none = false;
   int dev = 0, sms = 0;
-  int st = validate(M, N, K, A, lda, B, ldb, C, ldc, 2, &none, &dev, &sms);
+  int st = validate(M, N, K, false, false, A, lda, B, ldb, C, ldc, 2, &none, &dev, &sms);
   if (st != DGEMM_OK || none) return st;
   if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
-  return run_tc(dg::TcKind::kF16, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
+  return run_tc(dg::TcKind::kF16, false, false, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
+}
+
+int dgemm_gemm_ex(int path, int op_a, int op_b, int M, int N, int K, const void *A, int lda,
+                  const void *B, int ldb, float *C, int ldc, cudaStream_t stream) {
+  if (path < DGEMM_PATH_SIMT || path > DGEMM_PATH_FP16) return DGEMM_ERR_UNSUPPORTED;
+  if ((op_a != DGEMM_OP_N && op_a != DGEMM_OP_T) || (op_b != DGEMM_OP_N && op_b != DGEMM_OP_T))
+    return DGEMM_ERR_UNSUPPORTED;
+  const bool a_t = op_a == DGEMM_OP_T, b_t = op_b == DGEMM_OP_T;
+  const int es = (path == DGEMM_PATH_BF16 || path == DGEMM_PATH_FP16) ? 2 : 4;
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, a_t, b_t, A, lda, B, ldb, C, ldc, es, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  if (path == DGEMM_PATH_SIMT) {
+    const bool ab_vec = aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0;
+    const bool c_vec = aligned(C, 16) && ldc % 4 == 0;
+    return after_launch(dg::launch_simt(a_t, b_t, M, N, K, static_cast<const float *>(A), lda,
+                                        static_cast<const float *>(B), ldb, C, ldc, ab_vec,
+                                        c_vec, sms, stream),
+                        "SIMT GEMM launch");
+  }
+  const dg::TcKind kind = path == DGEMM_PATH_TF32    ? dg::TcKind::kTF32
+                          : path == DGEMM_PATH_3XTF32 ? dg::TcKind::k3xTF32
+                          : path == DGEMM_PATH_BF16   ? dg::TcKind::kBF16
+                                                      : dg::TcKind::kF16;
+  return run_tc(kind, a_t, b_t, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
 }
 
 const char *dgemm_status_string(int status) {

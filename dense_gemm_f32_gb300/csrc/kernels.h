@@ -11,9 +11,21 @@ namespace dg {
 // When the output tiles leave a last wave at most half full, those tiles
 // are split along K (partials in stream-ordered scratch, summed in a fixed
 // order by the last part to finish).
-cudaError_t launch_simt(int M, int N, int K, const float *A, int64_t lda, const float *B,
-                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec, int num_sms,
-                        cudaStream_t stream);
+// a_t: A is stored K x M (op(A) = A^T); b_t: B is stored N x K (op(B) = B^T).
+cudaError_t launch_simt(bool a_t, bool b_t, int M, int N, int K, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float *C, int64_t ldc, bool ab_vec,
+                        bool c_vec, int num_sms, cudaStream_t stream);
+
+// One operand layout each (unit u = 2 * a_t + b_t, one translation unit each).
+#define DG_DECLARE_SIMT_UNIT(u)                                                            \
+  cudaError_t launch_simt_unit_##u(int M, int N, int K, const float *A, int64_t lda,       \
+                                   const float *B, int64_t ldb, float *C, int64_t ldc,     \
+                                   bool ab_vec, bool c_vec, int num_sms, cudaStream_t stream);
+DG_DECLARE_SIMT_UNIT(0)
+DG_DECLARE_SIMT_UNIT(1)
+DG_DECLARE_SIMT_UNIT(2)
+DG_DECLARE_SIMT_UNIT(3)
+#undef DG_DECLARE_SIMT_UNIT
 
 // C[i*ldc + j] = 0 for i < M, j < N (the empty sum, K == 0).
 cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
@@ -22,12 +34,26 @@ cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
 // Element type of a tensor-core GEMM's operands.
 enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2, kF16 = 3 };
 
-// tcgen05 GEMM.  A (M x K) and B (K x N) row-major with leading dimensions in
-// elements; both must satisfy the TMA rules (16-byte aligned base, leading
-// dimension * element size a multiple of 16 bytes).  C fp32 row-major.
-cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
-                      const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
+// tcgen05 GEMM, C = op(A) op(B).  a_t: A is stored K x M (op(A) = A^T), else
+// M x K; b_t: B is stored N x K (op(B) = B^T), else K x N; all row-major with
+// leading dimensions in elements.  A and B must satisfy the TMA rules
+// (16-byte aligned base, leading dimension * element size a multiple of 16
+// bytes).  C fp32 row-major.
+cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
+                      int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
                       int num_sms, cudaStream_t stream);
+
+// One operand layout each (unit u = 2 * a_t + b_t, one translation unit each);
+// `watchdog` is the device address of the watchdog word.
+#define DG_DECLARE_TC_UNIT(u)                                                                 \
+  cudaError_t launch_tc_unit_##u(TcKind kind, int M, int N, int K, const void *A, int64_t lda, \
+                                 const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec, \
+                                 int num_sms, int *watchdog, cudaStream_t stream);
+DG_DECLARE_TC_UNIT(0)
+DG_DECLARE_TC_UNIT(1)
+DG_DECLARE_TC_UNIT(2)
+DG_DECLARE_TC_UNIT(3)
+#undef DG_DECLARE_TC_UNIT
 
 // Copy a rows x cols matrix of elem_bytes-sized elements (4 or 2) from
 // (src, lds) to (dst, ldd); used to re-pitch operands whose rows do not start

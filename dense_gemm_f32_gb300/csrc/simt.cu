@@ -27,9 +27,21 @@
 
 #include "kernels.h"
 
+// This file is compiled once per operand layout: DGEMM_SIMT_UNIT = 2 * AT + BT
+// (AT: A stored K x M; BT: B stored N x K), so the layouts compile in
+// parallel.  Unit 0 also holds the dispatch and the zero fill.
+#ifndef DGEMM_SIMT_UNIT
+#define DGEMM_SIMT_UNIT 0
+#endif
+#define DG_SCAT2(a, b) a##b
+#define DG_SCAT(a, b) DG_SCAT2(a, b)
+#define DG_SIMT_UNIT_LAUNCHER DG_SCAT(launch_simt_unit_, DGEMM_SIMT_UNIT)
+
 namespace dg {
 namespace {
 
+constexpr bool kUnitAT = (DGEMM_SIMT_UNIT >> 1) & 1;
+constexpr bool kUnitBT = DGEMM_SIMT_UNIT & 1;
 constexpr int kGroupM = 8;        // tile rows per raster group
 
 // Load 4 consecutive elements X[r][c..c+3] of an R x Cn row-major matrix,
@@ -61,6 +73,7 @@ struct SimtCfg {
   static constexpr int BM = BM_, BN = BN_, BK = BK_, WM = WM_, WN = WN_;
   static constexpr int LM = LM_, LN = 32 / LM_;
   static constexpr int AROW = BM + 4;                   // floats per As row (+4 pad)
+  static constexpr int BROW = BN + 4;                   // floats per Bs row (+4 pad)
   static constexpr int THREADS = WM * WN * 32;
   static constexpr int TM = BM / WM / LM, TN = BN / WN / LN;
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
@@ -69,10 +82,14 @@ struct SimtCfg {
   static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 blocks");
   static_assert(A_VECS >= 1 && B_VECS >= 1, "every thread loads A and B");
   static_assert(BM * BK % (4 * THREADS) == 0 && BK * BN % (4 * THREADS) == 0, "even loads");
-  static constexpr int SMEM_BYTES = 2 * BK * AROW * 4 + 2 * BK * BN * 4;  // two buffers
+  static constexpr int SMEM_BYTES = 2 * BK * AROW * 4 + 2 * BK * BROW * 4;  // two buffers
 };
 
-template <class G, bool kVec>
+// AT: A is stored K x M (op(A) = A^T); BT: B is stored N x K (op(B) = B^T).
+// Shared memory always holds A k-major and B n-major; a transposed A lands
+// there with plain 128-bit stores, a transposed B with transposing scalar
+// stores (the row pads keep both conflict-free).
+template <class G, bool kVec, bool AT, bool BT>
 __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     sgemm_simt_kernel(int M, int N, int K, const float *__restrict__ A, int64_t lda,
                       const float *__restrict__ B, int64_t ldb, float *__restrict__ C,
@@ -82,8 +99,8 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   // A stored k-major (transposed): a 128-bit load gives 4 consecutive rows.
   extern __shared__ float4 simt_smem[];
   auto As = reinterpret_cast<float(*)[BK][G::AROW]>(simt_smem);
-  auto Bs = reinterpret_cast<float(*)[BK][BN]>(reinterpret_cast<float *>(simt_smem) +
-                                                2 * BK * G::AROW);
+  auto Bs = reinterpret_cast<float(*)[BK][G::BROW]>(reinterpret_cast<float *>(simt_smem) +
+                                                      2 * BK * G::AROW);
 
   // ---- work unit -> (tile, K range).  Blocks below split_first each own a
   // whole tile; the tiles from split_first on (the last, partial wave) are
@@ -124,34 +141,54 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-  // global -> shared assignment: A as BM rows x BK/4 float4s, B as BK rows x BN/4
+  // global -> shared assignment, 128-bit vectors along each stored row:
+  // A: BM rows x BK/4 (stored M x K) or BK rows x BM/4 (stored K x M);
+  // B: BK rows x BN/4 (stored K x N) or BN rows x BK/4 (stored N x K).
   float4 ra[G::A_VECS], rb[G::B_VECS];
   auto load_tiles = [&](int k0) {
 #pragma unroll
     for (int v = 0; v < G::A_VECS; ++v) {
       const int e = tid + v * G::THREADS;
-      ra[v] = load4<kVec>(A, lda, m0 + e / (BK / 4), k0 + (e % (BK / 4)) * 4, M, K);
+      if constexpr (AT)
+        ra[v] = load4<kVec>(A, lda, k0 + e / (BM / 4), m0 + (e % (BM / 4)) * 4, K, M);
+      else
+        ra[v] = load4<kVec>(A, lda, m0 + e / (BK / 4), k0 + (e % (BK / 4)) * 4, M, K);
     }
 #pragma unroll
     for (int v = 0; v < G::B_VECS; ++v) {
       const int e = tid + v * G::THREADS;
-      rb[v] = load4<kVec>(B, ldb, k0 + e / (BN / 4), n0 + (e % (BN / 4)) * 4, K, N);
+      if constexpr (BT)
+        rb[v] = load4<kVec>(B, ldb, n0 + e / (BK / 4), k0 + (e % (BK / 4)) * 4, N, K);
+      else
+        rb[v] = load4<kVec>(B, ldb, k0 + e / (BN / 4), n0 + (e % (BN / 4)) * 4, K, N);
     }
   };
   auto store_tiles = [&](int buf) {
 #pragma unroll
     for (int v = 0; v < G::A_VECS; ++v) {
       const int e = tid + v * G::THREADS;
-      const int r = e / (BK / 4), c = (e % (BK / 4)) * 4;
-      As[buf][c + 0][r] = ra[v].x;
-      As[buf][c + 1][r] = ra[v].y;
-      As[buf][c + 2][r] = ra[v].z;
-      As[buf][c + 3][r] = ra[v].w;
+      if constexpr (AT) {
+        *reinterpret_cast<float4 *>(&As[buf][e / (BM / 4)][(e % (BM / 4)) * 4]) = ra[v];
+      } else {
+        const int r = e / (BK / 4), c = (e % (BK / 4)) * 4;
+        As[buf][c + 0][r] = ra[v].x;
+        As[buf][c + 1][r] = ra[v].y;
+        As[buf][c + 2][r] = ra[v].z;
+        As[buf][c + 3][r] = ra[v].w;
+      }
     }
 #pragma unroll
     for (int v = 0; v < G::B_VECS; ++v) {
       const int e = tid + v * G::THREADS;
-      *reinterpret_cast<float4 *>(&Bs[buf][e / (BN / 4)][(e % (BN / 4)) * 4]) = rb[v];
+      if constexpr (BT) {
+        const int r = e / (BK / 4), c = (e % (BK / 4)) * 4;
+        Bs[buf][c + 0][r] = rb[v].x;
+        Bs[buf][c + 1][r] = rb[v].y;
+        Bs[buf][c + 2][r] = rb[v].z;
+        Bs[buf][c + 3][r] = rb[v].w;
+      } else {
+        *reinterpret_cast<float4 *>(&Bs[buf][e / (BN / 4)][(e % (BN / 4)) * 4]) = rb[v];
+      }
     }
   };
 
@@ -252,13 +289,13 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   }
 }
 
-template <class G>
+template <class G, bool AT, bool BT>
 cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, const float *B,
                             int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
                             int num_sms, cudaStream_t stream) {
   const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
-  auto kern = ab_vec ? sgemm_simt_kernel<G, true> : sgemm_simt_kernel<G, false>;
+  auto kern = ab_vec ? sgemm_simt_kernel<G, true, AT, BT> : sgemm_simt_kernel<G, false, AT, BT>;
   if (G::SMEM_BYTES > 48 * 1024) {
     // opt in to more than 48 KB of dynamic shared memory (per device, once)
     static bool done[2][64] = {};
@@ -306,6 +343,7 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   return e;
 }
 
+#if DGEMM_SIMT_UNIT == 0
 __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ldc) {
   const int64_t total = (int64_t)M * N;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
@@ -314,17 +352,39 @@ __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ld
     C[r * ldc + c] = 0.f;
   }
 }
+#endif
 
 }  // namespace
 
 // The configuration the library ships (see the variant table in the design doc).
 using SimtShipped = SimtCfg<128, 256, 16, 2, 4, 8, 1>;
 
-cudaError_t launch_simt(int M, int N, int K, const float *A, int64_t lda, const float *B,
-                        int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec, int num_sms,
-                        cudaStream_t stream) {
-  const cudaError_t e = launch_simt_cfg<SimtShipped>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
-                                                     c_vec, num_sms, stream);
+// This unit's operand layout.
+cudaError_t DG_SIMT_UNIT_LAUNCHER(int M, int N, int K, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb, float *C, int64_t ldc, bool ab_vec,
+                                  bool c_vec, int num_sms, cudaStream_t stream) {
+  return launch_simt_cfg<SimtShipped, kUnitAT, kUnitBT>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
+                                                        c_vec, num_sms, stream);
+}
+
+#if DGEMM_SIMT_UNIT == 0
+cudaError_t launch_simt(bool a_t, bool b_t, int M, int N, int K, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float *C, int64_t ldc, bool ab_vec,
+                        bool c_vec, int num_sms, cudaStream_t stream) {
+  cudaError_t e;
+  switch ((a_t ? 2 : 0) + (b_t ? 1 : 0)) {
+    case 0:
+      e = launch_simt_unit_0(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, num_sms, stream);
+      break;
+    case 1:
+      e = launch_simt_unit_1(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, num_sms, stream);
+      break;
+    case 2:
+      e = launch_simt_unit_2(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, num_sms, stream);
+      break;
+    default:
+      e = launch_simt_unit_3(M, N, K, A, lda, B, ldb, C, ldc, ab_vec, c_vec, num_sms, stream);
+  }
   if (e == cudaSuccess) count_launch();
   return e;
 }
@@ -341,5 +401,6 @@ cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
   if (e == cudaSuccess) count_launch();
   return e;
 }
+#endif
 
 }  // namespace dg

@@ -34,12 +34,29 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+// This file is compiled once per operand layout: DGEMM_TC_UNIT = 2 * AT + BT
+// selects which kernels one translation unit instantiates (AT: A stored
+// K x M; BT: B stored N x K), so the four layouts compile in parallel.  Unit
+// 0 also holds the watchdog word, the re-pitch kernel and the dispatch.
+#ifndef DGEMM_TC_UNIT
+#define DGEMM_TC_UNIT 0
+#endif
+#define DG_CAT2(a, b) a##b
+#define DG_CAT(a, b) DG_CAT2(a, b)
+#define DG_UNIT_LAUNCHER DG_CAT(launch_tc_unit_, DGEMM_TC_UNIT)
+
 namespace dg {
 
+#if DGEMM_TC_UNIT == 0
 // Device watchdog word: 0, or the site code of the first wait that gave up.
+// Kernels of every unit receive its address as an argument.
 __device__ int g_watchdog = 0;
+#endif
 
 namespace {
+
+constexpr bool kUnitAT = (DGEMM_TC_UNIT >> 1) & 1;
+constexpr bool kUnitBT = DGEMM_TC_UNIT & 1;
 
 constexpr int BM = 128;
 
@@ -54,8 +71,12 @@ enum : int {
   kSiteSplitFull = 0x41,
 };
 
-template <TcKind KIND, int BN_>
+// AT: A is stored K x M (op(A) = A^T), read MN-major.  BT: B is stored N x K
+// (op(B) = B^T), read K-major.  The defaults are the row-major A (K-major)
+// and B (MN-major) of the plain product.
+template <TcKind KIND, int BN_, bool AT_ = false, bool BT_ = false>
 struct Cfg {
+  static constexpr bool AT = AT_, BT = BT_;
   // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
   static constexpr bool k16 = KIND == TcKind::kBF16 || KIND == TcKind::kF16;
   // operand format code of the instruction descriptor: F16 0, BF16 1, TF32 2
@@ -66,11 +87,16 @@ struct Cfg {
   static constexpr int BK = 128 / ES;             // k per stage: one 128-B swizzle row
   static constexpr int UMMA_K = 32 / ES;          // k per MMA instruction (32 bytes)
   static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per stage (per product)
-  static constexpr int BOX_N = 128 / ES;          // N columns per B box
-  static constexpr int B_BOXES = BN / BOX_N;
-  static constexpr int A_BYTES = BM * 128;        // 128 rows x 128 B
-  static constexpr int B_BOX_BYTES = BK * 128;    // BK rows x 128 B
-  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int BOX = 128 / ES;            // elements in one 128-byte swizzle row
+  static constexpr int BOX_N = BOX;               // N columns per MN-major B box
+  static constexpr int A_BYTES = BM * 128;        // 128 M x BK, either major
+  static constexpr int B_BYTES = BN * 128;        // BN N x BK, either major
+  // MN-major operands arrive as boxes of 128 bytes (of M or N) x BK rows;
+  // K-major operands as one box of BK x (rows).
+  static constexpr int A_BOXES = AT ? BM / BOX : 1;
+  static constexpr int A_BOX_BYTES = AT ? BK * 128 : A_BYTES;
+  static constexpr int B_BOXES = BT ? 1 : BN / BOX;
+  static constexpr int B_BOX_BYTES = BT ? B_BYTES : BK * 128;
   static constexpr int RAW_BYTES = A_BYTES + B_BYTES;               // what TMA writes
   static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);  // + lo copies
   static constexpr int STAGES = (kSplit ? 196608 : 196608) / STAGE_BYTES;
@@ -84,7 +110,7 @@ struct Cfg {
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
 
-  static_assert(BN % BOX_N == 0, "BN must be a whole number of B boxes");
+  static_assert(BN % BOX == 0 && BM % BOX == 0, "whole number of MN-major boxes");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
@@ -96,13 +122,15 @@ struct Cfg {
   // type 1, TMA mode SWIZZLE_128B_ATOM_32B).  Rows of a B box are contiguous
   // 128-byte lines, so the K-group stride is (group rows) x 128 B: 512 B
   // covers both a 4-row and an 8-row swizzle period for the 8-row MMA slice.
-  static constexpr uint32_t B_LAYOUT = k16 ? 2u : 1u;
-  static constexpr uint32_t B_SBO = k16 ? 1024u : 512u;
+  // MN-major swizzle: 128-byte rows of 16-byte chunks for 16-bit operands,
+  // 32-byte atoms for 32-bit ones (layout type 1); K-group stride 1024 / 512 B.
+  static constexpr uint32_t MN_LAYOUT = k16 ? 2u : 1u;
+  static constexpr uint32_t MN_SBO = k16 ? 1024u : 512u;
 
-  // Instruction descriptor: D fp32, A/B TF32 or BF16, A K-major, B MN-major,
-  // N >> 3 at bit 17, M >> 4 at bit 24.
-  static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) |
-                                    (kFmt << 10) | (0u << 15) | (1u << 16) |
+  // Instruction descriptor: D fp32, A/B format, A major (bit 15: 1 = MN),
+  // B major (bit 16: 1 = MN), N >> 3 at bit 17, M >> 4 at bit 24.
+  static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+                                    ((AT ? 1u : 0u) << 15) | ((BT ? 0u : 1u) << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 };
 
@@ -119,6 +147,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 // Tile id -> (tile row, tile col): tiles are walked in groups of `group_m`
 // tile rows, column by column inside a group, so that the CTAs working at the
 // same time share A row panels and B column panels in L2.
+// Descriptor of the k-th MMA slice (UMMA_K elements of K) of an operand tile
+// at saddr: K-major tiles advance 32 bytes inside the swizzle row; MN-major
+// tiles advance UMMA_K / 8 groups of 8 K-rows.  box_bytes is the distance
+// between the 128-byte MN blocks of an MN-major tile.
+template <class G, bool kMN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr, int k, uint32_t box_bytes) {
+  if constexpr (kMN)
+    return smem_desc(saddr + (uint32_t)(k * (G::UMMA_K / 8) * 1024), box_bytes, G::MN_SBO,
+                     G::MN_LAYOUT);
+  else
+    return smem_desc(saddr + (uint32_t)(k * 32), 16, 1024);
+}
+
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
                                             int &tm, int &tn) {
   const int per_group = group_m * tiles_n;
@@ -130,8 +171,8 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   tn = r / gsize;
 }
 
-__device__ __forceinline__ void watchdog_trip(int site, volatile int *abort_flag) {
-  atomicCAS(&g_watchdog, 0, site);
+__device__ __forceinline__ void watchdog_trip(int *watchdog, int site, volatile int *abort_flag) {
+  atomicCAS(watchdog, 0, site);
   *abort_flag = 1;
 }
 
@@ -148,12 +189,12 @@ __device__ __forceinline__ uint32_t split_lo_tf32(uint32_t xbits) {
   return l;
 }
 
-template <TcKind KIND, int BN>
-__global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
+template <TcKind KIND, int BN, bool AT, bool BT>
+__global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
-                   int N, int K, int64_t ldc, int c_vec, int group_m) {
-  using G = Cfg<KIND, BN>;
+                   int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog) {
+  using G = Cfg<KIND, BN, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -221,16 +262,27 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
         tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
-            if (!*abort_flag) watchdog_trip(kSiteProducerEmpty, abort_flag);
+            if (!*abort_flag) watchdog_trip(watchdog, kSiteProducerEmpty, abort_flag);
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
-          tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, tm * BM);
 #pragma unroll
-          for (int j = 0; j < G::B_BOXES; ++j)
-            tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
-                        tn * BN + j * G::BOX_N, kb * G::BK);
+          for (int j = 0; j < G::A_BOXES; ++j) {
+            if constexpr (AT)  // A stored K x M: boxes of BOX columns of M x BK rows
+              tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage),
+                          tm * BM + j * G::BOX, kb * G::BK);
+            else
+              tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, tm * BM);
+          }
+#pragma unroll
+          for (int j = 0; j < G::B_BOXES; ++j) {
+            if constexpr (BT)  // B stored N x K: one box of BK x BN
+              tma_load_2d(b_tile(stage), &tmap_b, full_bar(stage), kb * G::BK, tn * BN);
+            else
+              tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
+                          tn * BN + j * G::BOX_N, kb * G::BK);
+          }
           ++issued;
           if (++stage == G::STAGES) {
             stage = 0;
@@ -249,7 +301,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
             s = G::STAGES - 1;
             ph ^= 1u;
           }
-          if (!mbar_wait(full_bar(s), ph)) atomicCAS(&g_watchdog, 0, kSiteProducerDrain);
+          if (!mbar_wait(full_bar(s), ph)) atomicCAS(watchdog, 0, kSiteProducerDrain);
         }
       }
     }
@@ -263,7 +315,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
-          if (!*abort_flag) watchdog_trip(kSiteMmaAccEmpty, abort_flag);
+          if (!*abort_flag) watchdog_trip(watchdog, kSiteMmaAccEmpty, abort_flag);
           ok = false;
           break;
         }
@@ -272,25 +324,19 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t ready = G::kSplit ? split_bar(stage) : full_bar(stage);
           if (*abort_flag || !mbar_wait(ready, phase)) {
-            if (!*abort_flag) watchdog_trip(kSiteMmaFull, abort_flag);
+            if (!*abort_flag) watchdog_trip(watchdog, kSiteMmaFull, abort_flag);
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < G::KSTEPS; ++k) {
-            // A: K-major, advance 32 bytes per MMA inside the swizzle row.
-            // B: MN-major, advance UMMA_K rows = UMMA_K / 8 atoms of 1024 B.
-            const uint32_t a_off = (uint32_t)(k * 32);
-            const uint32_t b_off = (uint32_t)(k * (G::UMMA_K / 8) * 1024);
-            const uint64_t ad = smem_desc(a_tile(stage) + a_off, 16, 1024);
-            const uint64_t bd =
-                smem_desc(b_tile(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+            const uint64_t ad = operand_desc<G, AT>(a_tile(stage), k, G::A_BOX_BYTES);
+            const uint64_t bd = operand_desc<G, !BT>(b_tile(stage), k, G::B_BOX_BYTES);
             const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
             if constexpr (G::kSplit) {
-              const uint64_t adl = smem_desc(a_lo(stage) + a_off, 16, 1024);
-              const uint64_t bdl =
-                  smem_desc(b_lo(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+              const uint64_t adl = operand_desc<G, AT>(a_lo(stage), k, G::A_BOX_BYTES);
+              const uint64_t bdl = operand_desc<G, !BT>(b_lo(stage), k, G::B_BOX_BYTES);
               umma_tf32(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32(d_tmem, ad, bdl, G::IDESC, 1u);      // A_hi B_lo
               umma_tf32(d_tmem, ad, bd, G::IDESC, 1u);       // A_hi B_hi
@@ -316,7 +362,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
       // Drain: wait until every MMA issued above has completed before TMEM is
       // released (on the normal path the epilogue has already seen them all).
       umma_commit(drain_bar);
-      if (!mbar_wait(drain_bar, 0)) atomicCAS(&g_watchdog, 0, kSiteMmaDrain);
+      if (!mbar_wait(drain_bar, 0)) atomicCAS(watchdog, 0, kSiteMmaDrain);
     }
   } else if (warp < G::kEpiWarp0 + G::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
@@ -328,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
       tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
       // every lane waits, so that each one acquires the accumulator itself
       bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
-      if (!ok && lane == 0 && !*abort_flag) watchdog_trip(kSiteEpiAccFull, abort_flag);
+      if (!ok && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSiteEpiAccFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int row = tm * BM + quarter * 32 + lane;
@@ -372,7 +418,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
       for (int kb = 0; kb < kblocks; ++kb) {
         // every lane waits: each acquires the TMA-written bytes it reads
         bool got = !*abort_flag && mbar_wait(full_bar(stage), phase);
-        if (!got && lane == 0 && !*abort_flag) watchdog_trip(kSiteSplitFull, abort_flag);
+        if (!got && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSiteSplitFull, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -425,8 +471,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN>::THREADS, 1)
 //    releases the accumulator on the even CTA's barrier.
 //  * Before leaving, each CTA waits (bounded) for every signal still heading
 //    its way, then both CTAs meet at a cluster barrier and free TMEM.
-template <TcKind KIND>
+template <TcKind KIND, bool AT_ = false, bool BT_ = false>
 struct Cfg2 {
+  static constexpr bool AT = AT_, BT = BT_;
   // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
   static constexpr bool k16 = KIND == TcKind::kBF16 || KIND == TcKind::kF16;
   // operand format code of the instruction descriptor: F16 0, BF16 1, TF32 2
@@ -438,11 +485,14 @@ struct Cfg2 {
   static constexpr int BK = 128 / ES;
   static constexpr int UMMA_K = 32 / ES;
   static constexpr int KSTEPS = BK / UMMA_K;
-  static constexpr int BOX_N = 128 / ES;
-  static constexpr int B_BOXES = HN / BOX_N;
-  static constexpr int A_BYTES = HM * 128;
-  static constexpr int B_BOX_BYTES = BK * 128;
-  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int BOX = 128 / ES;            // elements in one 128-byte swizzle row
+  static constexpr int BOX_N = BOX;
+  static constexpr int A_BYTES = HM * 128;        // this CTA's 128 rows of M x BK
+  static constexpr int B_BYTES = HN * 128;        // this CTA's 128 columns of N x BK
+  static constexpr int A_BOXES = AT ? HM / BOX : 1;
+  static constexpr int A_BOX_BYTES = AT ? BK * 128 : A_BYTES;
+  static constexpr int B_BOXES = BT ? 1 : HN / BOX;
+  static constexpr int B_BOX_BYTES = BT ? B_BYTES : BK * 128;
   static constexpr int RAW_BYTES = A_BYTES + B_BYTES;                // per CTA, per stage
   static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);   // + lo copies (3xTF32)
   static constexpr int STAGES = 196608 / STAGE_BYTES;
@@ -458,10 +508,10 @@ struct Cfg2 {
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
-  static constexpr uint32_t B_LAYOUT = k16 ? 2u : 1u;
-  static constexpr uint32_t B_SBO = k16 ? 1024u : 512u;
-  static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) |
-                                    (kFmt << 10) | (0u << 15) | (1u << 16) |
+  static constexpr uint32_t MN_LAYOUT = k16 ? 2u : 1u;
+  static constexpr uint32_t MN_SBO = k16 ? 1024u : 512u;
+  static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+                                    ((AT ? 1u : 0u) << 15) | ((BT ? 0u : 1u) << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(kSplitWarp0 == 2 + kEpiWarps, "split warps follow the epilogue warps");
@@ -478,13 +528,13 @@ enum : int {
   kSite2SplitFull = 0x81,
 };
 
-template <TcKind KIND>
-__global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
+template <TcKind KIND, bool AT, bool BT>
+__global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_c, float *__restrict__ C, int M,
-                    int N, int K, int64_t ldc, int c_tma, int group_m) {
-  using G = Cfg2<KIND>;
+                    int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog) {
+  using G = Cfg2<KIND, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -556,29 +606,38 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
-            if (!*abort_flag) watchdog_trip(kSite2ProducerEmpty, abort_flag);
+            if (!*abort_flag) watchdog_trip(watchdog, kSite2ProducerEmpty, abort_flag);
             ok = false;
             break;
           }
-          const int ya = tm * G::BM + (int)rank * G::HM;
-          const int xb = tn * G::BN + (int)rank * G::HN;
+          const int m0 = tm * G::BM + (int)rank * G::HM;  // this CTA's rows of op(A)
+          const int n0 = tn * G::BN + (int)rank * G::HN;  // this CTA's columns of op(B)
+          // Box coordinates (x = inner, y = outer) of the j-th box of each operand.
+          auto ax = [&](int j) { return AT ? m0 + j * G::BOX : kb * G::BK; };
+          auto ay = [&](int j) { return AT ? kb * G::BK : m0; };
+          auto bx = [&](int j) { return BT ? kb * G::BK : n0 + j * G::BOX; };
+          auto by = [&](int j) { return BT ? n0 : kb * G::BK; };
           if constexpr (G::kSplit) {
             // each CTA's split warps wait on its own full barrier
             mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
-            tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, ya);
+#pragma unroll
+            for (int j = 0; j < G::A_BOXES; ++j)
+              tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage), ax(j),
+                          ay(j));
 #pragma unroll
             for (int j = 0; j < G::B_BOXES; ++j)
-              tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
-                          xb + j * G::BOX_N, kb * G::BK);
+              tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage), bx(j),
+                          by(j));
           } else {
             // both halves signal the even CTA's full barrier
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (uint32_t)G::RAW_BYTES);
-            tma_load_2d_pair(a_tile(stage), &tmap_a, fb, kb * G::BK, ya);
+#pragma unroll
+            for (int j = 0; j < G::A_BOXES; ++j)
+              tma_load_2d_pair(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, fb, ax(j), ay(j));
 #pragma unroll
             for (int j = 0; j < G::B_BOXES; ++j)
-              tma_load_2d_pair(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, fb, xb + j * G::BOX_N,
-                               kb * G::BK);
+              tma_load_2d_pair(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, fb, bx(j), by(j));
           }
           if (++stage == G::STAGES) {
             stage = 0;
@@ -591,7 +650,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
       // abort, that no copy is still writing this CTA's shared memory).
       for (int i = 0; i < G::STAGES; ++i) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
-          atomicCAS(&g_watchdog, 0, kSite2ProducerTail);
+          atomicCAS(watchdog, 0, kSite2ProducerTail);
           break;
         }
         if (++stage == G::STAGES) {
@@ -610,7 +669,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
         if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
-          if (!*abort_flag) watchdog_trip(kSite2MmaAccEmpty, abort_flag);
+          if (!*abort_flag) watchdog_trip(watchdog, kSite2MmaAccEmpty, abort_flag);
           ok = false;
           break;
         }
@@ -619,23 +678,19 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t ready = G::kSplit ? ready_bar(stage) : full_bar(stage);
           if (*abort_flag || !mbar_wait(ready, phase)) {
-            if (!*abort_flag) watchdog_trip(kSite2MmaFull, abort_flag);
+            if (!*abort_flag) watchdog_trip(watchdog, kSite2MmaFull, abort_flag);
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < G::KSTEPS; ++k) {
-            const uint32_t a_off = (uint32_t)(k * 32);
-            const uint32_t b_off = (uint32_t)(k * (G::UMMA_K / 8) * 1024);
-            const uint64_t ad = smem_desc(a_tile(stage) + a_off, 16, 1024);
-            const uint64_t bd =
-                smem_desc(b_tile(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+            const uint64_t ad = operand_desc<G, AT>(a_tile(stage), k, G::A_BOX_BYTES);
+            const uint64_t bd = operand_desc<G, !BT>(b_tile(stage), k, G::B_BOX_BYTES);
             const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
             if constexpr (G::kSplit) {
-              const uint64_t adl = smem_desc(a_lo(stage) + a_off, 16, 1024);
-              const uint64_t bdl =
-                  smem_desc(b_lo(stage) + b_off, G::B_BOX_BYTES, G::B_SBO, G::B_LAYOUT);
+              const uint64_t adl = operand_desc<G, AT>(a_lo(stage), k, G::A_BOX_BYTES);
+              const uint64_t bdl = operand_desc<G, !BT>(b_lo(stage), k, G::B_BOX_BYTES);
               umma_tf32_pair(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32_pair(d_tmem, ad, bdl, G::IDESC, 1u);     // A_hi B_lo
               umma_tf32_pair(d_tmem, ad, bd, G::IDESC, 1u);      // A_hi B_hi
@@ -659,12 +714,12 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
         }
       }
       umma_commit_pair(drain_bar, 0x1);
-      if (!mbar_wait(drain_bar, 0)) atomicCAS(&g_watchdog, 0, kSite2MmaDrain);
+      if (!mbar_wait(drain_bar, 0)) atomicCAS(watchdog, 0, kSite2MmaDrain);
       // Tail: both accumulators released by both epilogues, so that every
       // release signal from the odd CTA has landed before this CTA leaves.
       for (int i = 0; i < 2; ++i) {
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
-          atomicCAS(&g_watchdog, 0, kSite2MmaTail);
+          atomicCAS(watchdog, 0, kSite2MmaTail);
           break;
         }
         if (++acc == 2) {
@@ -685,7 +740,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
       int tm, tn;
       tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
       bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
-      if (!ok && lane == 0 && !*abort_flag) watchdog_trip(kSite2EpiAccFull, abort_flag);
+      if (!ok && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSite2EpiAccFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int row0 = tm * G::BM + (int)rank * G::HM + quarter * 32;
@@ -756,7 +811,7 @@ __global__ void __launch_bounds__(Cfg2<KIND>::THREADS, 1)
     for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
       for (int kb = 0; kb < kblocks; ++kb) {
         bool got = !*abort_flag && mbar_wait(full_bar(stage), phase);
-        if (!got && lane == 0 && !*abort_flag) watchdog_trip(kSite2SplitFull, abort_flag);
+        if (!got && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSite2SplitFull, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -842,22 +897,42 @@ int raster_group_m(int dflt) {
   return g ? g : dflt;
 }
 
-template <TcKind KIND, int BN>
+template <TcKind KIND>
+constexpr CUtensorMapDataType tma_type() {
+  return KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+         : KIND == TcKind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+// Tensor maps of A and B for configuration G, whose tiles hold `rows_a` rows
+// of op(A) and `cols_b` columns of op(B) per CTA.  K-major operands are read
+// as boxes of BK (one 128-byte swizzle row) x rows; MN-major operands as
+// boxes of 128 bytes of M or N x BK rows, with the 32-byte-atom swizzle for
+// 32-bit elements.
+template <class G, TcKind KIND>
+bool make_operand_maps(CUtensorMap *ta, CUtensorMap *tb, int M, int N, int K, const void *A,
+                       int64_t lda, const void *B, int64_t ldb, int rows_a, int cols_b) {
+  const CUtensorMapDataType dt = tma_type<KIND>();
+  const CUtensorMapSwizzle mn_swz =
+      G::k16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+  const bool ok_a = G::AT ? make_map(ta, A, dt, G::ES, K, M, lda, G::BOX, G::BK, mn_swz)
+                          : make_map(ta, A, dt, G::ES, M, K, lda, G::BK, rows_a,
+                                     CU_TENSOR_MAP_SWIZZLE_128B);
+  const bool ok_b = G::BT ? make_map(tb, B, dt, G::ES, N, K, ldb, G::BK, cols_b,
+                                     CU_TENSOR_MAP_SWIZZLE_128B)
+                          : make_map(tb, B, dt, G::ES, K, N, ldb, G::BOX, G::BK, mn_swz);
+  return ok_a && ok_b;
+}
+
+template <TcKind KIND, int BN, bool AT, bool BT>
 cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
-                       cudaStream_t stream) {
-  using G = Cfg<KIND, BN>;
-  const CUtensorMapDataType dt =
-      KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-      : KIND == TcKind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+                       int *watchdog, cudaStream_t stream) {
+  using G = Cfg<KIND, BN, AT, BT>;
   CUtensorMap ta, tb;
-  const CUtensorMapSwizzle b_swz =
-      G::k16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
-  if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN))
     return cudaErrorInvalidValue;
-  if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK, b_swz)) return cudaErrorInvalidValue;
-  auto kern = tc_gemm_kernel<KIND, BN>;
+  auto kern = tc_gemm_kernel<KIND, BN, AT, BT>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -871,31 +946,25 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
   kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                     raster_group_m(32));
+                                                     raster_group_m(32), watchdog);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
 }
 
-template <TcKind KIND>
+template <TcKind KIND, bool AT, bool BT>
 cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const void *B,
-                        int64_t ldb, float *C, int64_t ldc, bool c_vec, cudaStream_t stream) {
-  using G = Cfg2<KIND>;
-  const CUtensorMapDataType dt =
-      KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-      : KIND == TcKind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  const CUtensorMapSwizzle b_swz =
-      G::k16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int *watchdog,
+                        cudaStream_t stream) {
+  using G = Cfg2<KIND, AT, BT>;
   CUtensorMap ta, tb, tc;
-  if (!make_map(&ta, A, dt, G::ES, M, K, lda, G::BK, G::HM, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, G::HM, G::HN))
     return cudaErrorInvalidValue;
-  if (!make_map(&tb, B, dt, G::ES, K, N, ldb, G::BOX_N, G::BK, b_swz)) return cudaErrorInvalidValue;
   // C through TMA stores when its rows start on 16-byte boundaries.
   memset(&tc, 0, sizeof(tc));
   const bool c_tma = c_vec && make_map(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32,
                                        32, CU_TENSOR_MAP_SWIZZLE_128B);
-  auto kern = tc2_gemm_kernel<KIND>;
+  auto kern = tc2_gemm_kernel<KIND, AT, BT>;
   static int max_clusters[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -926,7 +995,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   cfg.gridDim = dim3(2 * clusters);
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, C, M, N, K, ldc, c_tma ? 1 : 0,
-                         raster_group_m(16));
+                         raster_group_m(16), watchdog);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
@@ -944,6 +1013,18 @@ bool use_pair(int M, int N, int num_sms) {
   return pair_tiles * 4 >= num_sms;
 }
 
+template <TcKind KIND, int BN1>
+cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const void *B,
+                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
+                        int *watchdog, cudaStream_t stream) {
+  constexpr bool AT = kUnitAT, BT = kUnitBT;
+  if (use_pair(M, N, num_sms))
+    return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream);
+  return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
+                                       stream);
+}
+
+#if DGEMM_TC_UNIT == 0
 __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_bytes,
                                uint8_t *__restrict__ dst, int64_t ldd_bytes, int rows,
                                int64_t row_bytes, int64_t pad_bytes, int es) {
@@ -968,35 +1049,63 @@ __global__ void read_watchdog_kernel(int *out) {
   *out = g_watchdog;
   g_watchdog = 0;
 }
+#endif
 
 }  // namespace
 
-cudaError_t launch_tc(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
-                      const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                      int num_sms, cudaStream_t stream) {
+// This unit's layout: every tensor-core kind with AT = kUnitAT, BT = kUnitBT.
+cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
+                             const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
+                             int num_sms, int *watchdog, cudaStream_t stream) {
   switch (kind) {
     case TcKind::kTF32:
-      if (use_pair(M, N, num_sms))
-        return launch_cfg2<TcKind::kTF32>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
-      return launch_cfg<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            stream);
+      return launch_kind<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                             watchdog, stream);
     case TcKind::k3xTF32:
-      if (use_pair(M, N, num_sms))
-        return launch_cfg2<TcKind::k3xTF32>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
-      return launch_cfg<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                              stream);
+      return launch_kind<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                               watchdog, stream);
     case TcKind::kBF16:
-      if (use_pair(M, N, num_sms))
-        return launch_cfg2<TcKind::kBF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
-      return launch_cfg<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            stream);
+      return launch_kind<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                             watchdog, stream);
     case TcKind::kF16:
-      if (use_pair(M, N, num_sms))
-        return launch_cfg2<TcKind::kF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, stream);
-      return launch_cfg<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                           stream);
+      return launch_kind<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                            watchdog, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+#if DGEMM_TC_UNIT == 0
+namespace {
+// Device address of this device's watchdog word (looked up once per device).
+int *watchdog_address() {
+  static int *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_watchdog) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int *>(p);
+  }
+  return addr[dev];
+}
+}  // namespace
+
+cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
+                      int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
+                      int num_sms, cudaStream_t stream) {
+  int *wd = watchdog_address();
+  if (wd == nullptr) return cudaErrorInvalidSymbol;
+  const int unit = (a_t ? 2 : 0) + (b_t ? 1 : 0);
+  switch (unit) {
+    case 0:
+      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+    case 1:
+      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+    case 2:
+      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+    default:
+      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+  }
 }
 
 cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
@@ -1029,5 +1138,6 @@ cudaError_t read_watchdog(cudaStream_t stream, int *code) {
   if (e == cudaSuccess) *code = h;
   return e;
 }
+#endif
 
 }  // namespace dg

@@ -70,6 +70,21 @@ typedef enum {
     DGEMM_ERR_SCRATCH_LIMIT = 10   /* gemm_f32_tc_noalloc: operands need more than its fixed scratch */
 } dgemm_status_t;
 
+/* Operand operations of dgemm_gemm_ex: op(X) = X or its transpose. */
+typedef enum {
+    DGEMM_OP_N = 0,  /* as stored */
+    DGEMM_OP_T = 1   /* transposed */
+} dgemm_op_t;
+
+/* Arithmetic paths of dgemm_gemm_ex (element type of A and B in brackets). */
+typedef enum {
+    DGEMM_PATH_SIMT = 0,    /* FP32 FFMA on the CUDA cores       [fp32] */
+    DGEMM_PATH_TF32 = 1,    /* tcgen05, TF32 operands            [fp32] */
+    DGEMM_PATH_3XTF32 = 2,  /* tcgen05, split-precision 3xTF32   [fp32] */
+    DGEMM_PATH_BF16 = 3,    /* tcgen05, BF16 operands            [bf16] */
+    DGEMM_PATH_FP16 = 4     /* tcgen05, FP16 operands            [fp16] */
+} dgemm_path_t;
+
 /* Tensor-core precision modes of gemm_f32_tc. */
 typedef enum {
     DGEMM_TC_TF32 = 0,   /* operands read at TF32 precision (10-bit mantissa), FP32 accumulate */
@@ -195,6 +210,31 @@ int gemm_f16_tc(int M, int N, int K,
                 const unsigned short *B, int ldb,
                 float *C, int ldc,
                 cudaStream_t stream);
+
+/*
+ * dgemm_gemm_ex -- C = op(A) x op(B) on any path, with transposed operands.
+ *
+ * Lesson 8 section 二十八 ("矩阵布局为什么重要") describes row- and column-major
+ * storage and the transpose flags that GEMM interfaces carry for them.  Here
+ * every matrix is stored row-major; a transposed operand is simply stored
+ * with its other dimension contiguous (a column-major op(X) is a row-major
+ * X^T):
+ *   op_a = DGEMM_OP_N: A is M x K, lda >= max(1, K);  op(A) = A
+ *   op_a = DGEMM_OP_T: A is K x M, lda >= max(1, M);  op(A) = A^T
+ *   op_b = DGEMM_OP_N: B is K x N, ldb >= max(1, N);  op(B) = B
+ *   op_b = DGEMM_OP_T: B is N x K, ldb >= max(1, K);  op(B) = B^T
+ * C is M x N fp32, row-major, ldc >= max(1, N); C[i][j] = sum_k op(A)[i][k]
+ * op(B)[k][j].  `path` (dgemm_path_t) selects the arithmetic and the element
+ * type of A and B; accuracy, semantics and status codes are those of the
+ * corresponding entry point above (gemm_f32_simt, gemm_f32_tc, gemm_bf16_tc,
+ * gemm_f16_tc), which equal dgemm_gemm_ex with op_a = op_b = DGEMM_OP_N.
+ * Unknown path or op: DGEMM_ERR_UNSUPPORTED.
+ */
+int dgemm_gemm_ex(int path, int op_a, int op_b, int M, int N, int K,
+                  const void *A, int lda,
+                  const void *B, int ldb,
+                  float *C, int ldc,
+                  cudaStream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char *dgemm_status_string(int status);

@@ -135,3 +135,33 @@ def _caller(fn):
     if fn == "fp16":
         return lambda *a: dg.gemm_f16_tc(*a, 0)
     return lambda *a: dg.gemm_bf16_tc(*a, 0)
+
+
+@pytest.mark.parametrize("path", range(5))
+def test_gemm_ex_leading_dimensions_follow_the_stored_shape(lib, path):
+    """op_a = T: A is stored K x M, so lda >= M; op_b = T: B is N x K, ldb >= K."""
+    call = lambda oa, ob, *a: dg.dgemm_gemm_ex(path, oa, ob, *a, 0)  # noqa: E731
+    E = dg.ERR_INVALID_VALUE
+    N_, T_ = dg.OP_N, dg.OP_T
+    # M=8, N=16, K=4: A^T stored 4 x 8 needs lda >= 8; B^T stored 16 x 4 needs ldb >= 4
+    assert call(T_, N_, 8, 16, 4, P, 4, P * 2, 16, P * 4, 16) == E
+    assert call(N_, T_, 8, 16, 4, P, 4, P * 2, 3, P * 4, 16) == E
+    assert call(N_, N_, 8, 16, 4, P, 3, P * 2, 16, P * 4, 16) == E
+    # C overlapping A's stored span (4 rows of 8 when transposed)
+    es = 2 if path >= 3 else 4
+    assert call(T_, N_, 8, 16, 4, P, 8, P * 4, 16, P + 2 * 8 * es, 16) == dg.ERR_ALIAS
+
+
+def test_gemm_ex_rejects_unknown_path_or_op(lib):
+    assert dg.dgemm_gemm_ex(5, 0, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.dgemm_gemm_ex(-1, 0, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.dgemm_gemm_ex(1, 2, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.dgemm_gemm_ex(1, 0, -1, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.dgemm_gemm_ex(1, 0, 1, 0, 4, 4, 0, 4, 0, 4, 0, 4, 0) == dg.OK
+
+
+def test_matmul_transposed_shape_checks_need_no_gpu():
+    import torch
+
+    with pytest.raises(ValueError):
+        dg.matmul(torch.zeros(3, 2), torch.zeros(3, 4), mode="simt", trans_a=False)
