@@ -52,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--layout", choices=["NN", "NT", "TN", "TT"], default="NN",
+                   help="operand layout of the headline: T = that operand is stored transposed "
+                        "(A as K x M, B as N x K)")
     p.add_argument("--shape", default=None,
                    help="M,N,K: time the headline mode on a seeded uniform[-1,1) workload of this "
                         "shape instead of the benchmark workload (profiling runs)")
@@ -333,7 +336,7 @@ def device_inputs(w, mode, device):
     return A, B, A.to(device), B.to(device)
 
 
-def time_device(mode, Ad, Bd, C, steps, warmup, dist, device):
+def time_device(mode, Ad, Bd, C, steps, warmup, dist, device, ta=False, tb=False):
     """Device time of `steps` back-to-back calls (inputs resident in HBM)."""
     import torch
 
@@ -341,7 +344,7 @@ def time_device(mode, Ad, Bd, C, steps, warmup, dist, device):
 
     stream = torch.cuda.current_stream(device)
     for _ in range(warmup):
-        dg.matmul(Ad, Bd, mode=mode, out=C)
+        dg.matmul(Ad, Bd, mode=mode, out=C, trans_a=ta, trans_b=tb)
     torch.cuda.synchronize(device)
     dist.barrier()
     torch.cuda.synchronize(device)
@@ -350,7 +353,7 @@ def time_device(mode, Ad, Bd, C, steps, warmup, dist, device):
     w0 = time.time()
     for i in range(steps):
         ev[i].record(stream)
-        dg.matmul(Ad, Bd, mode=mode, out=C)
+        dg.matmul(Ad, Bd, mode=mode, out=C, trans_a=ta, trans_b=tb)
     ev[steps].record(stream)
     torch.cuda.synchronize(device)
     w1 = time.time()
@@ -440,8 +443,13 @@ def run_ours(args, dist):
     mode = args.mode
     w = workload_for(mode, shape=args.shape)
     A, B, Ad, Bd = device_inputs(w, mode, device)
+    ta, tb = args.layout[0] == "T", args.layout[1] == "T"
+    if ta:  # store the transposed operands (A as K x M, B as N x K)
+        Ad = Ad.t().contiguous()
+    if tb:
+        Bd = Bd.t().contiguous()
     C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
-    r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device)
+    r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device, ta, tb)
     agg = aggregate(r["ms_total"], dist.world, w.flops, args.steps, lambda x: dist.max(x, device))
     windows = [r["window"]]
     launches_per_step = r["launches"] / args.steps
@@ -508,7 +516,8 @@ def run_ours(args, dist):
                       "fp16": "fp16"}[mode],
             "data": "synthetic (seeded, shapes and distributions of the workload)",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "mode": mode,
-                       "layout": "row-major, compact leading dimensions",
+                       "layout": f"row-major, compact leading dimensions, op(A) op(B) = "
+                                 f"{args.layout}",
                        "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": "replicas" if dist.world > 1 else "single GPU"},
             "roofline": roofline,
