@@ -133,6 +133,51 @@ int validate(int M, int N, int K, bool a_t, bool b_t, const void *A, int lda, co
   return DGEMM_OK;
 }
 
+}  // namespace
+
+// ------------------------------------------------------------------------
+// Scratch: a library-owned stream-ordered memory pool per device.  Freed
+// scratch stays reserved in the pool (up to kPoolKeepBytes) so that the next
+// call's allocation is a pool hit instead of a trip to the driver.
+namespace dg {
+namespace {
+constexpr uint64_t kPoolKeepBytes = 256ull << 20;
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pools[64] = {};
+}  // namespace
+
+cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (g_pools[dev] == nullptr) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t p = nullptr;
+      if ((e = cudaMemPoolCreate(&p, &props)) != cudaSuccess) return e;
+      uint64_t keep = kPoolKeepBytes;
+      if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+        cudaMemPoolDestroy(p);
+        return e;
+      }
+      g_pools[dev] = p;
+    }
+    pool = g_pools[dev];
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
+cudaError_t scratch_free(void *ptr, cudaStream_t stream) { return cudaFreeAsync(ptr, stream); }
+}  // namespace dg
+
+namespace {
+
 int after_launch(cudaError_t e, const char *what) {
   if (e != cudaSuccess) return cuda_fail(e, what);
   return DGEMM_OK;
@@ -159,8 +204,8 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
     const int64_t ldb2 = (b_cols + pitch_elems - 1) / pitch_elems * pitch_elems;
     const size_t a_bytes = a_ok ? 0 : (size_t)((int64_t)a_rows * lda2 * es + 255) / 256 * 256;
     const size_t b_bytes = b_ok ? 0 : (size_t)((int64_t)b_rows * ldb2 * es + 255) / 256 * 256;
-    e = cudaMallocAsync(&scratch, a_bytes + b_bytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (re-pitch scratch)");
+    e = dg::scratch_alloc(&scratch, a_bytes + b_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scratch allocation (re-pitch)");
     char *s = static_cast<char *>(scratch);
     if (!a_ok) {
       e = dg::launch_repitch(A, lda, s, lda2, a_rows, a_cols, es, num_sms, stream);
@@ -176,11 +221,11 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
     }
   }
   e = dg::launch_tc(kind, a_t, b_t, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
-                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, /*allow_split=*/true, stream);
 done:
   if (scratch != nullptr) {
-    cudaError_t e2 = cudaFreeAsync(scratch, stream);
-    if (e == cudaSuccess && e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+    cudaError_t e2 = dg::scratch_free(scratch, stream);
+    if (e == cudaSuccess && e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
   }
   return after_launch(e, "tensor-core GEMM launch");
 }
@@ -209,7 +254,7 @@ int noalloc_scratch(int dev, void **ptr) {
   return DGEMM_OK;
 }
 
-// run_tc with the fixed scratch array in place of cudaMallocAsync.
+// run_tc with the fixed scratch array in place of the scratch pool.
 int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda, const float *B,
                    int ldb, float *C, int ldc, int dev, int num_sms, cudaStream_t stream) {
   const int es = 4;
@@ -242,7 +287,7 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
     }
   }
   e = dg::launch_tc(kind, false, false, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
-                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, /*allow_split=*/false, stream);
   return after_launch(e, "tensor-core GEMM launch (no-alloc)");
 }
 

@@ -325,7 +325,7 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
     split_first = tiles - rem;
     grid = split_first + rem * parts;
     const size_t work_bytes = (size_t)(rem * parts) * G::BM * G::BN * sizeof(float);
-    e = cudaMallocAsync(&scratch, work_bytes + (size_t)rem * sizeof(unsigned int), stream);
+    e = scratch_alloc(&scratch, work_bytes + (size_t)rem * sizeof(unsigned int), stream);
     if (e != cudaSuccess) return e;
     work = static_cast<float *>(scratch);
     counters = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + work_bytes);
@@ -337,7 +337,7 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
     e = cudaGetLastError();
   }
   if (scratch) {
-    const cudaError_t e2 = cudaFreeAsync(scratch, stream);
+    const cudaError_t e2 = scratch_free(scratch, stream);
     if (e == cudaSuccess) e = e2;
   }
   return e;

@@ -193,7 +193,8 @@ template <TcKind KIND, int BN, bool AT, bool BT>
 __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
-                   int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog) {
+                   int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
+                   int splits, float *__restrict__ work) {
   using G = Cfg<KIND, BN, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -222,6 +223,13 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
   const int tiles_n = (N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + G::BK - 1) / G::BK;
+  // Work units: each tile split along K into `splits` parts (1 = whole
+  // tiles); the host picks splits so that every part has k-blocks.
+  const int units = num_tiles * splits;
+  const int per = (kblocks + splits - 1) / splits;
+  auto unit_tile = [&](int u) { return u / splits; };
+  auto unit_kb0 = [&](int u) { return min(kblocks, (u % splits) * per); };
+  auto unit_kb1 = [&](int u) { return min(kblocks, (u % splits) * per + per); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::STAGES; ++s) {
@@ -257,10 +265,10 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
       uint32_t phase = 0;
       int issued = 0;  // stages loaded so far (for the drain on abort)
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         int tm, tn;
-        tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        tile_coords(unit_tile(u), tiles_m, tiles_n, group_m, tm, tn);
+        for (int kb = unit_kb0(u); kb < unit_kb1(u); ++kb) {
           if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
             if (!*abort_flag) watchdog_trip(watchdog, kSiteProducerEmpty, abort_flag);
             ok = false;
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
           if (!*abort_flag) watchdog_trip(watchdog, kSiteMmaAccEmpty, abort_flag);
           ok = false;
@@ -321,7 +329,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const int kb0 = unit_kb0(u);
+        for (int kb = kb0; kb < unit_kb1(u); ++kb) {
           const uint32_t ready = G::kSplit ? split_bar(stage) : full_bar(stage);
           if (*abort_flag || !mbar_wait(ready, phase)) {
             if (!*abort_flag) watchdog_trip(watchdog, kSiteMmaFull, abort_flag);
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
           for (int k = 0; k < G::KSTEPS; ++k) {
             const uint64_t ad = operand_desc<G, AT>(a_tile(stage), k, G::A_BOX_BYTES);
             const uint64_t bd = operand_desc<G, !BT>(b_tile(stage), k, G::B_BOX_BYTES);
-            const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
             if constexpr (G::kSplit) {
               const uint64_t adl = operand_desc<G, AT>(a_lo(stage), k, G::A_BOX_BYTES);
               const uint64_t bdl = operand_desc<G, !BT>(b_lo(stage), k, G::B_BOX_BYTES);
@@ -369,16 +378,22 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
       int tm, tn;
-      tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+      tile_coords(unit_tile(u), tiles_m, tiles_n, group_m, tm, tn);
       // every lane waits, so that each one acquires the accumulator itself
       bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
       if (!ok && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSiteEpiAccFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
+      // A K-split part writes its partial tile into slice `part` of `work`
+      // (M x N each, leading dimension N); a separate pass sums the slices.
+      const bool to_work = splits > 1;
+      float *dst = to_work ? work + (int64_t)(u % splits) * M * N : C;
+      const int64_t ldd = to_work ? (int64_t)N : ldc;
+      const bool d_vec = to_work ? (N % 4 == 0) : (c_vec != 0);
       const int row = tm * BM + quarter * 32 + lane;
-      float *crow = C + (int64_t)row * ldc;
+      float *crow = dst + (int64_t)row * ldd;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -387,7 +402,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         tmem_wait_ld();
         const int col = tn * BN + c0;
         if (row < M) {
-          if (c_vec && col + 32 <= N) {
+          if (d_vec && col + 32 <= N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
               *reinterpret_cast<float4 *>(crow + col + j) =
@@ -414,8 +429,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < kblocks; ++kb) {
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int kb = unit_kb0(u); kb < unit_kb1(u); ++kb) {
         // every lane waits: each acquires the TMA-written bytes it reads
         bool got = !*abort_flag && mbar_wait(full_bar(stage), phase);
         if (!got && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSiteSplitFull, abort_flag);
@@ -927,7 +942,7 @@ bool make_operand_maps(CUtensorMap *ta, CUtensorMap *tb, int M, int N, int K, co
 template <TcKind KIND, int BN, bool AT, bool BT>
 cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
-                       int *watchdog, cudaStream_t stream) {
+                       int *watchdog, bool allow_split, cudaStream_t stream) {
   using G = Cfg<KIND, BN, AT, BT>;
   CUtensorMap ta, tb;
   if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN))
@@ -943,12 +958,39 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
+  // K-split for problems with fewer tiles than half the SMs: up to 8 parts
+  // of at least 4 k-blocks each, every part non-empty.
+  const int kblocks = (K + G::BK - 1) / G::BK;
+  int splits = 1;
+  const char *env = getenv("DGEMM_TC_SPLITK");  // "0" disables (tests and tuning)
+  if (env && env[0] == '0') allow_split = false;
+  if (allow_split && tiles * 2 <= num_sms) {
+    int s = (int)(num_sms / tiles);
+    s = s < 8 ? s : 8;
+    s = s < kblocks / 4 ? s : kblocks / 4;
+    if (s >= 2) {
+      const int per = (kblocks + s - 1) / s;
+      splits = (kblocks + per - 1) / per;
+    }
+  }
+  float *work = nullptr;
+  if (splits > 1) {
+    e = scratch_alloc(reinterpret_cast<void **>(&work),
+                      (size_t)splits * (size_t)M * (size_t)N * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t units = tiles * splits;
+  const int grid = (int)(units < num_sms ? units : num_sms);
   kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                     raster_group_m(32), watchdog);
+                                                     raster_group_m(32), watchdog, splits, work);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
+  if (work != nullptr) {
+    if (e == cudaSuccess) e = launch_splitk_reduce(work, splits, M, N, C, ldc, c_vec, num_sms, stream);
+    const cudaError_t e2 = scratch_free(work, stream);
+    if (e == cudaSuccess) e = e2;
+  }
   return e;
 }
 
@@ -1016,12 +1058,12 @@ bool use_pair(int M, int N, int num_sms) {
 template <TcKind KIND, int BN1>
 cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const void *B,
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
-                        int *watchdog, cudaStream_t stream) {
+                        int *watchdog, bool allow_split, cudaStream_t stream) {
   constexpr bool AT = kUnitAT, BT = kUnitBT;
   if (use_pair(M, N, num_sms))
     return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream);
   return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
-                                       stream);
+                                       allow_split, stream);
 }
 
 #if DGEMM_TC_UNIT == 0
@@ -1045,6 +1087,34 @@ __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_byte
   }
 }
 
+// C = sum of the K-split slices of `work` (each M x N, leading dimension N),
+// added in slice order so the result does not depend on scheduling.
+__global__ void splitk_reduce_kernel(const float *__restrict__ work, int splits, int M, int N,
+                                     float *__restrict__ C, int64_t ldc, int vec) {
+  const int64_t slice = (int64_t)M * N;
+  if (vec) {  // N % 4 == 0 and C rows 16-byte aligned: float4 per thread
+    const int64_t total = slice / 4;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+      float4 sum = __ldcs(reinterpret_cast<const float4 *>(work) + e);
+      for (int p = 1; p < splits; ++p) {
+        const float4 v = __ldcs(reinterpret_cast<const float4 *>(work + p * slice) + e);
+        sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
+      }
+      const int64_t r = (e * 4) / N, c = (e * 4) - r * N;
+      *reinterpret_cast<float4 *>(C + r * ldc + c) = sum;
+    }
+  } else {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < slice;
+         e += (int64_t)gridDim.x * blockDim.x) {
+      float sum = __ldcs(work + e);
+      for (int p = 1; p < splits; ++p) sum += __ldcs(work + p * slice + e);
+      const int64_t r = e / N, c = e - r * N;
+      C[r * ldc + c] = sum;
+    }
+  }
+}
+
 __global__ void read_watchdog_kernel(int *out) {
   *out = g_watchdog;
   g_watchdog = 0;
@@ -1056,20 +1126,20 @@ __global__ void read_watchdog_kernel(int *out) {
 // This unit's layout: every tensor-core kind with AT = kUnitAT, BT = kUnitBT.
 cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
                              const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                             int num_sms, int *watchdog, cudaStream_t stream) {
+                             int num_sms, int *watchdog, bool allow_split, cudaStream_t stream) {
   switch (kind) {
     case TcKind::kTF32:
       return launch_kind<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, stream);
+                                             watchdog, allow_split, stream);
     case TcKind::k3xTF32:
       return launch_kind<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                               watchdog, stream);
+                                               watchdog, allow_split, stream);
     case TcKind::kBF16:
       return launch_kind<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, stream);
+                                             watchdog, allow_split, stream);
     case TcKind::kF16:
       return launch_kind<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            watchdog, stream);
+                                            watchdog, allow_split, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -1092,19 +1162,23 @@ int *watchdog_address() {
 
 cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
                       int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                      int num_sms, cudaStream_t stream) {
+                      int num_sms, bool allow_split, cudaStream_t stream) {
   int *wd = watchdog_address();
   if (wd == nullptr) return cudaErrorInvalidSymbol;
   const int unit = (a_t ? 2 : 0) + (b_t ? 1 : 0);
   switch (unit) {
     case 0:
-      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
+                              allow_split, stream);
     case 1:
-      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
+                              allow_split, stream);
     case 2:
-      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
+                              allow_split, stream);
     default:
-      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
+                              allow_split, stream);
   }
 }
 
@@ -1123,16 +1197,29 @@ cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd,
   return e;
 }
 
+cudaError_t launch_splitk_reduce(const float *work, int splits, int M, int N, float *C,
+                                 int64_t ldc, bool c_vec, int num_sms, cudaStream_t stream) {
+  const int vec = (c_vec && N % 4 == 0) ? 1 : 0;
+  const int64_t items = vec ? (int64_t)M * N / 4 : (int64_t)M * N;
+  int64_t blocks = (items + 255) / 256;
+  if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+  if (blocks < 1) blocks = 1;
+  splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(work, splits, M, N, C, ldc, vec);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
 cudaError_t read_watchdog(cudaStream_t stream, int *code) {
   int *d = nullptr;
-  cudaError_t e = cudaMallocAsync(&d, sizeof(int), stream);
+  cudaError_t e = scratch_alloc(reinterpret_cast<void **>(&d), sizeof(int), stream);
   if (e != cudaSuccess) return e;
   read_watchdog_kernel<<<1, 1, 0, stream>>>(d);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   int h = 0;
   if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(int), cudaMemcpyDeviceToHost, stream);
-  cudaError_t e2 = cudaFreeAsync(d, stream);
+  cudaError_t e2 = scratch_free(d, stream);
   if (e == cudaSuccess) e = e2;
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e == cudaSuccess) *code = h;

@@ -38,12 +38,15 @@
  *   - A launch failure, or a sticky error left by earlier work, is returned as
  *     DGEMM_ERR_CUDA; dgemm_last_cuda_error() gives the CUDA message.
  *   - Deterministic: the same inputs give bitwise identical C on every call
- *     (no atomics, no split-K races).
+ *     (no floating-point atomics; K-split partial tiles are added in a fixed
+ *     order).
  *   - Thread-safe and re-entrant; the only mutable library state is a
  *     per-thread error string and a per-device watchdog word (see
  *     dgemm_watchdog_status).
- *   - Some paths use temporary device memory, taken with cudaMallocAsync /
- *     cudaFreeAsync on `stream` (stream-ordered, nothing kept between calls).
+ *   - Some paths use temporary device memory (re-pitched operands, K-split
+ *     partials): stream-ordered allocations on `stream` from a memory pool
+ *     the library creates per device, which keeps up to 256 MiB of freed
+ *     scratch reserved for the next calls.
  */
 #ifndef DGEMM_H
 #define DGEMM_H
