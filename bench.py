@@ -7,7 +7,10 @@ kernel with its loads, MMAs and epilogue).  The headline line times the
 TF32 tensor-core path at M = N = K = 8192; the same run also times every
 other mode (FP32 SIMT and 3xTF32 at 8192^3, BF16 and TF32 at the
 16384 x 14336 x 4096 transformer-layer shape) and reports them under
-"modes".  Inputs are larger than L2 (129 MB), so no flush is needed.
+"modes".  Inputs are larger than L2 (129 MB), so no flush is needed.  The
+small workloads (64^3, 1024^3, ragged 1000 x 1013 x 997) are timed per mode
+under "small", with L2 warm (CUDA-graph replay) and with L2 flushed before
+each call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--mode tf32|3xtf32|simt|bf16]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -336,8 +339,19 @@ def device_inputs(w, mode, device):
     return A, B, A.to(device), B.to(device)
 
 
-def time_device(mode, Ad, Bd, C, steps, warmup, dist, device, ta=False, tb=False):
-    """Device time of `steps` back-to-back calls (inputs resident in HBM)."""
+def l2_flush_buffer(device):
+    """A float32 buffer of twice the L2 size: writing it evicts A, B and C."""
+    import torch
+
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (129 << 20)
+    return torch.empty(2 * l2 // 4, dtype=torch.float32, device=device)
+
+
+def time_device(mode, Ad, Bd, C, steps, warmup, dist, device, ta=False, tb=False, flush=None):
+    """Device time of `steps` calls on inputs resident in HBM.  Without
+    `flush` the calls run back to back and are timed by one event between
+    each pair of calls; with it (inputs smaller than L2) the buffer is
+    rewritten before every call, outside that call's event pair."""
     import torch
 
     import dense_gemm_f32_gb300 as dg
@@ -349,20 +363,93 @@ def time_device(mode, Ad, Bd, C, steps, warmup, dist, device, ta=False, tb=False
     dist.barrier()
     torch.cuda.synchronize(device)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if flush is not None else None
     n0 = dg.dgemm_kernel_launches()
     w0 = time.time()
     for i in range(steps):
+        if flush is not None:
+            flush.zero_()
         ev[i].record(stream)
         dg.matmul(Ad, Bd, mode=mode, out=C, trans_a=ta, trans_b=tb)
+        if flush is not None:
+            ev_end[i].record(stream)
     ev[steps].record(stream)
     torch.cuda.synchronize(device)
     w1 = time.time()
     dist.barrier()
     torch.cuda.synchronize(device)
     launches = dg.dgemm_kernel_launches() - n0
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
-    total = ev[0].elapsed_time(ev[steps])
-    return {"ms_total": total, "per_step_ms": per, "launches": launches, "window": (w0, w1)}
+    if flush is None:
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        total = ev[0].elapsed_time(ev[steps])
+    else:
+        per = [ev[i].elapsed_time(ev_end[i]) for i in range(steps)]
+        total = sum(per)
+    return {"ms_total": total, "per_step_ms": per, "launches": launches, "window": (w0, w1),
+            "flushed": None if flush is None else True}
+
+
+def time_graph(mode, Ad, Bd, C, device, calls=20, replays=5):
+    """Device time per call of `calls` back-to-back calls captured in one CUDA
+    graph (no host launch gaps; L2 warm after the first call)."""
+    import torch
+
+    import dense_gemm_f32_gb300 as dg
+
+    st = torch.cuda.Stream(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        dg.matmul(Ad, Bd, mode=mode, out=C)
+        st.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            for _ in range(calls):
+                dg.matmul(Ad, Bd, mode=mode, out=C)
+    g.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(device)
+    e0.record(cur)
+    for _ in range(replays):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) * 1e3 / (calls * replays)
+
+
+SMALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16")
+
+
+def time_small(device, dist, steps=20):
+    """The small workloads of the benchmark configuration (64^3, 1024^3 and
+    the ragged 1000 x 1013 x 997), every mode: microseconds per call with L2
+    warm (graph replay of back-to-back calls) and with L2 flushed before each
+    call (event pair per call)."""
+    import torch
+
+    from dense_gemm_f32_gb300 import inputs
+
+    flush = l2_flush_buffer(device)
+    out, windows = {}, []
+    for w in (inputs.SQUARE_64, inputs.SQUARE_1024, inputs.RAGGED_1000):
+        for m in SMALL_MODES:
+            _, _, Ad, Bd = device_inputs(w, m, device)
+            C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
+            try:
+                warm = time_graph(m, Ad, Bd, C, device)
+            except RuntimeError as e:  # capture refused: report, keep going
+                warm = None
+                print(f"graph timing of {m}@{w.name} failed: {e}", file=sys.stderr)
+            r = time_device(m, Ad, Bd, C, steps, 3, dist, device, flush=flush)
+            windows.append(r["window"])
+            cold = statistics.median(r["per_step_ms"]) * 1e3
+            out[f"{m}@{w.name}"] = {
+                "us_warm": None if warm is None else round(warm, 2),
+                "us_l2_flushed": round(cold, 2),
+                "tflops_warm": None if warm is None else round(w.flops / warm / 1e6, 2),
+                "tflops_l2_flushed": round(w.flops / cold / 1e6, 2)}
+    del flush
+    torch.cuda.empty_cache()
+    return out, windows
 
 
 def time_e2e(mode, A, B, steps, warmup, dist, device):
@@ -449,7 +536,11 @@ def run_ours(args, dist):
     if tb:
         Bd = Bd.t().contiguous()
     C = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
-    r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device, ta, tb)
+    in_bytes = Ad.numel() * Ad.element_size() + Bd.numel() * Bd.element_size() + C.numel() * 4
+    l2 = getattr(props, "L2_cache_size", 0) or (129 << 20)
+    flush = l2_flush_buffer(device) if in_bytes < 2 * l2 else None
+    r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device, ta, tb, flush=flush)
+    del flush
     agg = aggregate(r["ms_total"], dist.world, w.flops, args.steps, lambda x: dist.max(x, device))
     windows = [r["window"]]
     launches_per_step = r["launches"] / args.steps
@@ -497,6 +588,10 @@ def run_ours(args, dist):
             modes[f"{m}@{wm.name}"] = {"tflops_median": round(tfl, 2), "bound": bm,
                                        "peak": round(pm, 1), "frac": round(tfl / pm, 4),
                                        "ms_median": round(res["ms_per_step"], 4)}
+    small = {}
+    if not args.no_modes and not args.shape:
+        small, sw = time_small(device, dist)
+        windows += sw
     clocks = summarize_clocks(sampler.stop(), windows)
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
@@ -518,7 +613,8 @@ def run_ours(args, dist):
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "mode": mode,
                        "layout": f"row-major, compact leading dimensions, op(A) op(B) = "
                                  f"{args.layout}",
-                       "l2": "inputs larger than L2 (no flush needed)",
+                       "l2": ("inputs larger than L2 (no flush needed)" if r.get("flushed") is None
+                              else "L2 flushed (2 x L2 bytes written) before every timed call"),
                        "parallelism": "replicas" if dist.world > 1 else "single GPU"},
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -526,6 +622,7 @@ def run_ours(args, dist):
             "gpu_launches": r["launches"],
             "clocks": clocks,
             "modes": modes,
+            "small": small,
             "step_ms": {"median": statistics.median(r["per_step_ms"]),
                         "min": min(r["per_step_ms"]), "max": max(r["per_step_ms"])},
         }

@@ -221,7 +221,7 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
     }
   }
   e = dg::launch_tc(kind, a_t, b_t, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
-                    aligned(C, 16) && (ldc % 4) == 0, num_sms, /*allow_split=*/true, stream);
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
 done:
   if (scratch != nullptr) {
     cudaError_t e2 = dg::scratch_free(scratch, stream);
@@ -287,7 +287,7 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
     }
   }
   e = dg::launch_tc(kind, false, false, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
-                    aligned(C, 16) && (ldc % 4) == 0, num_sms, /*allow_split=*/false, stream);
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
   return after_launch(e, "tensor-core GEMM launch (no-alloc)");
 }
 

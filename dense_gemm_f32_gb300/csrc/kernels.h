@@ -39,19 +39,18 @@ enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2, kF16 = 3 };
 // leading dimensions in elements.  A and B must satisfy the TMA rules
 // (16-byte aligned base, leading dimension * element size a multiple of 16
 // bytes).  C fp32 row-major.
-// allow_split: small problems may split tiles along K, with partials in
-// stream-ordered scratch (false: allocate nothing).
+// Problems with few tiles split them along K across thread-block clusters;
+// nothing is allocated.
 cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
                       int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                      int num_sms, bool allow_split, cudaStream_t stream);
+                      int num_sms, cudaStream_t stream);
 
 // One operand layout each (unit u = 2 * a_t + b_t, one translation unit each);
 // `watchdog` is the device address of the watchdog word.
 #define DG_DECLARE_TC_UNIT(u)                                                                 \
   cudaError_t launch_tc_unit_##u(TcKind kind, int M, int N, int K, const void *A, int64_t lda, \
                                  const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec, \
-                                 int num_sms, int *watchdog, bool allow_split,          \
-                                 cudaStream_t stream);
+                                 int num_sms, int *watchdog, cudaStream_t stream);
 DG_DECLARE_TC_UNIT(0)
 DG_DECLARE_TC_UNIT(1)
 DG_DECLARE_TC_UNIT(2)
@@ -71,11 +70,6 @@ cudaError_t scratch_free(void *ptr, cudaStream_t stream);
 
 // Count one successful kernel launch (dgemm_kernel_launches).
 void count_launch();
-
-// C = sum over p < splits of slice p of `work` (M x N each, leading dimension
-// N), in slice order.
-cudaError_t launch_splitk_reduce(const float *work, int splits, int M, int N, float *C,
-                                 int64_t ldc, bool c_vec, int num_sms, cudaStream_t stream);
 
 // Read and clear the device's watchdog word after synchronising `stream`.
 cudaError_t read_watchdog(cudaStream_t stream, int *code);

@@ -213,6 +213,23 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Loads from the shared::cluster window (this CTA's or a peer's shared
+// memory).  Volatile, so they stay between the cluster barriers around them.
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in a
 // peer CTA), with release semantics at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

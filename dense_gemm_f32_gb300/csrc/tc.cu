@@ -21,8 +21,14 @@
 //    box with zeros (the pages' zero-fill of partial tiles, section 二十六).
 //  * Accumulators: fp32 in tensor memory, two buffers of BN columns each, so
 //    the epilogue of tile i overlaps the main loop of tile i + 1.
+//  * Problems with too few tiles to occupy the GPU split each tile along K
+//    over a thread-block cluster of 2-8 CTAs: every CTA accumulates one K
+//    range, parks its partial tile in its own shared memory, and the CTAs then
+//    add the partials across the cluster (distributed shared memory) in part
+//    order, each CTA writing a slice of the tile's rows to C.
 //  * Every wait is bounded (ptx.cuh); on a timeout the CTA records the site in
 //    the device watchdog word, drains what it issued, frees TMEM and returns.
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -109,12 +115,18 @@ struct Cfg {
   // barriers: full[S], empty[S], split[S], acc_full[2], acc_empty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
+  // K-split: the partial 128 x BN tile parked in the (then idle) stage area,
+  // rows padded by 4 floats so that the epilogue's 16-byte row stores from 8
+  // consecutive lanes fall in distinct banks.
+  static constexpr int PART_PITCH = BN + 4;
+  static constexpr int MAX_SPLITS = 8;  // portable cluster size
 
   static_assert(BN % BOX == 0 && BM % BOX == 0, "whole number of MN-major boxes");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
   static_assert(kSplitWarp0 == kEpiWarp0 + kEpiWarps, "split warps follow the epilogue warps");
+  static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage area");
 
   // B (MN-major) layout.  16-bit operands use the plain 128-byte swizzle
   // (16-byte chunks permuted within each 128-byte row); 32-bit MN-major
@@ -194,7 +206,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
                    int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
-                   int splits, float *__restrict__ work) {
+                   int splits) {
   using G = Cfg<KIND, BN, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -224,7 +236,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K + G::BK - 1) / G::BK;
   // Work units: each tile split along K into `splits` parts (1 = whole
-  // tiles); the host picks splits so that every part has k-blocks.
+  // tiles); the host picks splits so that every part has k-blocks.  With
+  // splits > 1 the launch is one unit per CTA in clusters of `splits` CTAs,
+  // so a cluster's CTAs hold the parts of one tile and CTA rank = part.
   const int units = num_tiles * splits;
   const int per = (kblocks + splits - 1) / splits;
   auto unit_tile = [&](int u) { return u / splits; };
@@ -386,15 +400,29 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
       if (!ok && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSiteEpiAccFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // A K-split part writes its partial tile into slice `part` of `work`
-      // (M x N each, leading dimension N); a separate pass sums the slices.
-      const bool to_work = splits > 1;
-      float *dst = to_work ? work + (int64_t)(u % splits) * M * N : C;
-      const int64_t ldd = to_work ? (int64_t)N : ldc;
-      const bool d_vec = to_work ? (N % 4 == 0) : (c_vec != 0);
-      const int row = tm * BM + quarter * 32 + lane;
-      float *crow = dst + (int64_t)row * ldd;
+      const int trow = quarter * 32 + lane;  // this thread's accumulator row
+      const int row = tm * BM + trow;
+      float *crow = C + (int64_t)row * ldc;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      if (splits > 1) {
+        // K-split part: park the partial tile in shared memory.  Every MMA of
+        // the unit has completed (accf), so the stage area is no longer read
+        // by the tensor core nor written by TMA.
+        float *prow = reinterpret_cast<float *>(smem) + trow * G::PART_PITCH;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(prow + c0 + j) =
+                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        }
+        tc_fence_before();
+        break;  // one unit per CTA
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
@@ -402,7 +430,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         tmem_wait_ld();
         const int col = tn * BN + c0;
         if (row < M) {
-          if (d_vec && col + 32 <= N) {
+          if (c_vec && col + 32 <= N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
               *reinterpret_cast<float4 *>(crow + col + j) =
@@ -457,6 +485,55 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         }
       }
     }
+  }
+
+  if (splits > 1) {
+    // ---------------------------------------- K-split: cluster reduction
+    // Every thread of every CTA reaches both cluster barriers, also after a
+    // bounded wait gave up (the role loops above all end).
+    __syncwarp();
+    cluster_sync();  // partials written (release) and visible (acquire)
+    bool aborted = false;
+    for (int p = 0; p < splits; ++p)
+      aborted |= ld_cluster_s32(mapa_shared(smem_u32(const_cast<int *>(abort_flag)),
+                                            (uint32_t)p)) != 0;
+    if (!aborted) {
+      int tm, tn;
+      tile_coords(unit_tile(blockIdx.x), tiles_m, tiles_n, group_m, tm, tn);
+      const int rank = (int)cluster_ctarank();
+      const int r0 = (BM * rank) / splits, r1 = (BM * (rank + 1)) / splits;
+      constexpr int Q = BN / 4;  // float4s per tile row
+      uint32_t part[G::MAX_SPLITS];
+#pragma unroll
+      for (int p = 0; p < G::MAX_SPLITS; ++p)
+        part[p] = p < splits ? mapa_shared(base, (uint32_t)p) : 0u;
+      for (int e = threadIdx.x; e < (r1 - r0) * Q; e += blockDim.x) {
+        const int trow = r0 + e / Q, c = 4 * (e % Q);
+        const uint32_t off = (uint32_t)((trow * G::PART_PITCH + c) * 4);
+        float4 v[G::MAX_SPLITS];
+#pragma unroll
+        for (int p = 0; p < G::MAX_SPLITS; ++p)
+          if (p < splits) v[p] = ld_cluster_f4(part[p] + off);
+        float4 sum = v[0];  // parts added in K order
+#pragma unroll
+        for (int p = 1; p < G::MAX_SPLITS; ++p)
+          if (p < splits) sum.x += v[p].x, sum.y += v[p].y, sum.z += v[p].z, sum.w += v[p].w;
+        const int row = tm * BM + trow, col = tn * BN + c;
+        if (row < M) {
+          float *d = C + (int64_t)row * ldc + col;
+          if (c_vec && col + 4 <= N) {
+            *reinterpret_cast<float4 *>(d) = sum;
+          } else {
+            if (col < N) d[0] = sum.x;
+            if (col + 1 < N) d[1] = sum.y;
+            if (col + 2 < N) d[2] = sum.z;
+            if (col + 3 < N) d[3] = sum.w;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while a peer may still read its partial
   }
 
   tc_fence_before();
@@ -939,10 +1016,67 @@ bool make_operand_maps(CUtensorMap *ta, CUtensorMap *tb, int M, int N, int K, co
   return ok_a && ok_b;
 }
 
+// Clusters of `size` CTAs of `kern` that can be resident at once on device
+// `dev` (queried once per kernel, device and size).
+template <class Kern>
+int active_clusters(Kern kern, int threads, int smem, int dev, int size) {
+  static std::atomic<int> cache[64][9] = {};
+  if (dev < 0 || dev >= 64 || size < 1 || size > 8) return 0;
+  int n = cache[dev][size].load(std::memory_order_relaxed);
+  if (n == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)size, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 0) {
+      cudaGetLastError();  // not sticky; treat as "does not fit"
+      n = 0;
+    }
+    cache[dev][size].store(n > 0 ? n : -1, std::memory_order_relaxed);
+  }
+  return n > 0 ? n : 0;
+}
+
+// Parts per tile for the single-CTA kernel.  A problem whose tiles would
+// leave more than half the SMs idle splits each tile along K into up to 8
+// parts of at least 4 k-blocks (every part non-empty), the largest count whose
+// clusters are all resident at once.  DGEMM_TC_SPLITK=0 disables the split;
+// DGEMM_TC_SPLITK=2..8 forces that many parts (as far as the k-blocks allow;
+// clusters that do not fit run in waves), for tests and tuning.
+template <class Kern>
+int choose_splits(Kern kern, int threads, int smem, int dev, int64_t tiles, int kblocks,
+                  int num_sms) {
+  auto whole = [&](int s) {  // parts actually used when aiming for s
+    const int per = (kblocks + s - 1) / s;
+    return (kblocks + per - 1) / per;
+  };
+  const char *env = getenv("DGEMM_TC_SPLITK");
+  if (env && env[0] >= '0' && env[0] <= '8' && env[1] == 0) {
+    const int f = env[0] - '0';
+    return f >= 2 && kblocks >= 2 ? whole(f < kblocks ? f : kblocks) : 1;
+  }
+  if (tiles * 2 > num_sms) return 1;
+  int s = (int)(num_sms / tiles);
+  s = s < 8 ? s : 8;
+  s = s < kblocks / 4 ? s : kblocks / 4;
+  for (; s >= 2; --s) {
+    const int w = whole(s);
+    if (tiles <= (int64_t)active_clusters(kern, threads, smem, dev, w)) return w;
+  }
+  return 1;
+}
+
 template <TcKind KIND, int BN, bool AT, bool BT>
 cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
-                       int *watchdog, bool allow_split, cudaStream_t stream) {
+                       int *watchdog, cudaStream_t stream) {
   using G = Cfg<KIND, BN, AT, BT>;
   CUtensorMap ta, tb;
   if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN))
@@ -959,38 +1093,31 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   }
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
-  // K-split for problems with fewer tiles than half the SMs: up to 8 parts
-  // of at least 4 k-blocks each, every part non-empty.
   const int kblocks = (K + G::BK - 1) / G::BK;
-  int splits = 1;
-  const char *env = getenv("DGEMM_TC_SPLITK");  // "0" disables (tests and tuning)
-  if (env && env[0] == '0') allow_split = false;
-  if (allow_split && tiles * 2 <= num_sms) {
-    int s = (int)(num_sms / tiles);
-    s = s < 8 ? s : 8;
-    s = s < kblocks / 4 ? s : kblocks / 4;
-    if (s >= 2) {
-      const int per = (kblocks + s - 1) / s;
-      splits = (kblocks + per - 1) / per;
-    }
-  }
-  float *work = nullptr;
+  const int splits = choose_splits(kern, G::THREADS, G::SMEM_BYTES, dev, tiles, kblocks, num_sms);
   if (splits > 1) {
-    e = scratch_alloc(reinterpret_cast<void **>(&work),
-                      (size_t)splits * (size_t)M * (size_t)N * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
+    // one unit per CTA, the `splits` parts of a tile in one cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles * splits), 1, 1);
+    cfg.blockDim = dim3(G::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m(32),
+                           watchdog, splits);
+  } else {
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
+                                                       raster_group_m(32), watchdog, 1);
+    e = cudaGetLastError();
   }
-  const int64_t units = tiles * splits;
-  const int grid = (int)(units < num_sms ? units : num_sms);
-  kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                     raster_group_m(32), watchdog, splits, work);
-  e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
-  if (work != nullptr) {
-    if (e == cudaSuccess) e = launch_splitk_reduce(work, splits, M, N, C, ldc, c_vec, num_sms, stream);
-    const cudaError_t e2 = scratch_free(work, stream);
-    if (e == cudaSuccess) e = e2;
-  }
   return e;
 }
 
@@ -1058,12 +1185,11 @@ bool use_pair(int M, int N, int num_sms) {
 template <TcKind KIND, int BN1>
 cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const void *B,
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
-                        int *watchdog, bool allow_split, cudaStream_t stream) {
+                        int *watchdog, cudaStream_t stream) {
   constexpr bool AT = kUnitAT, BT = kUnitBT;
   if (use_pair(M, N, num_sms))
     return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream);
-  return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
-                                       allow_split, stream);
+  return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog, stream);
 }
 
 #if DGEMM_TC_UNIT == 0
@@ -1087,34 +1213,6 @@ __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_byte
   }
 }
 
-// C = sum of the K-split slices of `work` (each M x N, leading dimension N),
-// added in slice order so the result does not depend on scheduling.
-__global__ void splitk_reduce_kernel(const float *__restrict__ work, int splits, int M, int N,
-                                     float *__restrict__ C, int64_t ldc, int vec) {
-  const int64_t slice = (int64_t)M * N;
-  if (vec) {  // N % 4 == 0 and C rows 16-byte aligned: float4 per thread
-    const int64_t total = slice / 4;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-      float4 sum = __ldcs(reinterpret_cast<const float4 *>(work) + e);
-      for (int p = 1; p < splits; ++p) {
-        const float4 v = __ldcs(reinterpret_cast<const float4 *>(work + p * slice) + e);
-        sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
-      }
-      const int64_t r = (e * 4) / N, c = (e * 4) - r * N;
-      *reinterpret_cast<float4 *>(C + r * ldc + c) = sum;
-    }
-  } else {
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < slice;
-         e += (int64_t)gridDim.x * blockDim.x) {
-      float sum = __ldcs(work + e);
-      for (int p = 1; p < splits; ++p) sum += __ldcs(work + p * slice + e);
-      const int64_t r = e / N, c = e - r * N;
-      C[r * ldc + c] = sum;
-    }
-  }
-}
-
 __global__ void read_watchdog_kernel(int *out) {
   *out = g_watchdog;
   g_watchdog = 0;
@@ -1126,20 +1224,20 @@ __global__ void read_watchdog_kernel(int *out) {
 // This unit's layout: every tensor-core kind with AT = kUnitAT, BT = kUnitBT.
 cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
                              const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                             int num_sms, int *watchdog, bool allow_split, cudaStream_t stream) {
+                             int num_sms, int *watchdog, cudaStream_t stream) {
   switch (kind) {
     case TcKind::kTF32:
       return launch_kind<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, allow_split, stream);
+                                             watchdog, stream);
     case TcKind::k3xTF32:
       return launch_kind<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                               watchdog, allow_split, stream);
+                                               watchdog, stream);
     case TcKind::kBF16:
       return launch_kind<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, allow_split, stream);
+                                             watchdog, stream);
     case TcKind::kF16:
       return launch_kind<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            watchdog, allow_split, stream);
+                                            watchdog, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -1162,23 +1260,19 @@ int *watchdog_address() {
 
 cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
                       int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                      int num_sms, bool allow_split, cudaStream_t stream) {
+                      int num_sms, cudaStream_t stream) {
   int *wd = watchdog_address();
   if (wd == nullptr) return cudaErrorInvalidSymbol;
   const int unit = (a_t ? 2 : 0) + (b_t ? 1 : 0);
   switch (unit) {
     case 0:
-      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
-                              allow_split, stream);
+      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
     case 1:
-      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
-                              allow_split, stream);
+      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
     case 2:
-      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
-                              allow_split, stream);
+      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
     default:
-      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd,
-                              allow_split, stream);
+      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
   }
 }
 
@@ -1192,19 +1286,6 @@ cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd,
       static_cast<const uint8_t *>(src), lds * elem_bytes, static_cast<uint8_t *>(dst),
       ldd * elem_bytes, rows, (int64_t)cols * elem_bytes, (ldd - cols) * (int64_t)elem_bytes,
       elem_bytes);
-  const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) count_launch();
-  return e;
-}
-
-cudaError_t launch_splitk_reduce(const float *work, int splits, int M, int N, float *C,
-                                 int64_t ldc, bool c_vec, int num_sms, cudaStream_t stream) {
-  const int vec = (c_vec && N % 4 == 0) ? 1 : 0;
-  const int64_t items = vec ? (int64_t)M * N / 4 : (int64_t)M * N;
-  int64_t blocks = (items + 255) / 256;
-  if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
-  if (blocks < 1) blocks = 1;
-  splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(work, splits, M, N, C, ldc, vec);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;

@@ -43,8 +43,8 @@
  *   - Thread-safe and re-entrant; the only mutable library state is a
  *     per-thread error string and a per-device watchdog word (see
  *     dgemm_watchdog_status).
- *   - Some paths use temporary device memory (re-pitched operands, K-split
- *     partials): stream-ordered allocations on `stream` from a memory pool
+ *   - Some paths use temporary device memory (re-pitched operands, the FP32
+ *     SIMT path's K-split partials): stream-ordered allocations on `stream` from a memory pool
  *     the library creates per device, which keeps up to 256 MiB of freed
  *     scratch reserved for the next calls.
  */

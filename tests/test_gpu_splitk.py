@@ -1,13 +1,16 @@
 """K-split of the single-CTA tensor-core kernel.
 
-When a problem has too few 128 x 256 output tiles to fill half the GPU, the
-single-CTA kernel divides each tile's K range into parts (at most 8, each at
-least 4 k-blocks), writes one fp32 partial tile per part to scratch, and a
-second kernel adds the parts in a fixed order into C.  DGEMM_TC_SPLITK=0
-turns the split off.  These tests run shapes that split evenly, unevenly and
-not at all, with and without the split, against the CPU oracle, and check that
-the split result does not depend on the order the parts finish in.
+When a problem has too few 128 x BN output tiles to fill half the GPU, the
+single-CTA kernel divides each tile's K range into parts (2 to 8, each at
+least 4 k-blocks) and runs the parts of one tile as one thread-block cluster.
+Every CTA parks its partial tile in its own shared memory; after a cluster
+barrier the CTAs add the partials in part order through distributed shared
+memory, each writing a slice of the tile's rows to C.  DGEMM_TC_SPLITK=0
+turns the split off and DGEMM_TC_SPLITK=n (2..8) forces n parts.  These tests
+run every cluster size and the automatic choice against the CPU oracle, and
+check that the split result does not depend on scheduling.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -35,14 +38,14 @@ def _single_cta(monkeypatch):
     monkeypatch.setenv("DGEMM_TC_PAIR", "0")
 
 
-# (M, N, K): one tile with 8 parts; 34 k-blocks of fp32 (7 uneven parts);
+# (M, N, K): one tile with 8 parts; 34 fp32 k-blocks (7 uneven parts);
 # 32 tiles (4 parts); too short a K to split; a ragged tile grid.
 SHAPES = [(128, 256, 1000), (100, 200, 1061), (1024, 1024, 1024), (300, 500, 96),
           (333, 777, 2345)]
 
 
 @pytest.mark.parametrize("mode", TC_MODES)
-def test_split_and_unsplit_match_oracle(mode, monkeypatch):
+def test_automatic_split_and_unsplit_match_oracle(mode, monkeypatch):
     for (M, N, K) in SHAPES:
         A, B = inputs.make_random(M, N, K, seed=M + N + K, dist="normal",
                                   dtype=gu.in_dtype(mode))
@@ -59,23 +62,38 @@ def test_split_and_unsplit_match_oracle(mode, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", TC_MODES)
-def test_split_adds_one_reduce_launch(mode, monkeypatch):
-    """A split call launches the GEMM kernel and the reduce kernel; an unsplit
-    call launches the GEMM kernel alone."""
+@pytest.mark.parametrize("parts", [2, 3, 4, 5, 6, 7, 8])
+def test_every_cluster_size(mode, parts, monkeypatch):
+    """Forced part counts, so every cluster size and every row slicing of
+    the 128-row tile (128 / parts need not be whole) runs; ragged M, N, K;
+    more clusters than fit at once for the larger sizes."""
+    monkeypatch.setenv("DGEMM_TC_SPLITK", str(parts))
+    for (M, N, K) in [(200, 300, 777), (1300, 700, 515)]:
+        A, B = inputs.make_random(M, N, K, seed=parts * 1000 + M, dist="normal",
+                                  dtype=gu.in_dtype(mode))
+        Ad, Bd = A.cuda(), B.cuda()
+        C1 = gu.run(mode, Ad, Bd).clone()
+        C2 = gu.run(mode, Ad, Bd)
+        assert torch.equal(C1, C2)
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(C1.cpu().numpy(), ref, S, gu.TOL[mode], f"{mode} parts={parts} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("mode", TC_MODES)
+def test_split_is_one_launch(mode, monkeypatch):
+    """The split needs no second kernel and no scratch."""
     A, B = inputs.make_random(128, 256, 1000, seed=5, dtype=gu.in_dtype(mode))
     Ad, Bd = A.cuda(), B.cuda()
-    n0 = dg.dgemm_kernel_launches()
-    gu.run(mode, Ad, Bd)
-    assert dg.dgemm_kernel_launches() - n0 == 2
-    monkeypatch.setenv("DGEMM_TC_SPLITK", "0")
-    n0 = dg.dgemm_kernel_launches()
-    gu.run(mode, Ad, Bd)
-    assert dg.dgemm_kernel_launches() - n0 == 1
+    for env in ("8", "0"):
+        monkeypatch.setenv("DGEMM_TC_SPLITK", env)
+        n0 = dg.dgemm_kernel_launches()
+        gu.run(mode, Ad, Bd)
+        assert dg.dgemm_kernel_launches() - n0 == 1
 
 
 @pytest.mark.parametrize("mode", TC_MODES)
 def test_split_guard_bands_and_unaligned_ldc(mode):
-    """The reduce kernel writes C through an ldc that breaks 16-byte row
+    """The cluster reduction writes C through an ldc that breaks 16-byte row
     alignment (scalar stores) and leaves the gap columns untouched."""
     M, N, K = 301, 517, 2000
     A, B = inputs.make_random(M, N, K, seed=33, dist="normal", dtype=gu.in_dtype(mode))
@@ -87,14 +105,28 @@ def test_split_guard_bands_and_unaligned_ldc(mode):
         gu.assert_guards_intact(buf, M, N, ldc)
 
 
-@pytest.mark.parametrize("mode", ["tf32", "bf16"])
-def test_split_integer_bit_exact(mode):
+@pytest.mark.parametrize("mode", TC_MODES)
+def test_split_transposed_operands(mode, monkeypatch):
+    """The split with A stored K x M and B stored N x K."""
+    monkeypatch.setenv("DGEMM_TC_SPLITK", "4")
+    M, N, K = 260, 390, 1100
+    A, B = inputs.make_random(M, N, K, seed=77, dist="normal", dtype=gu.in_dtype(mode))
+    At, Bt = A.t().contiguous().cuda(), B.t().contiguous().cuda()
+    C = dg.matmul(At, Bt, mode=mode, trans_a=True, trans_b=True)
+    torch.cuda.synchronize()
+    ref, S = gu.oracle_full(A, B)
+    gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL[mode], f"{mode} split TT")
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16", "3xtf32"])
+def test_split_integer_bit_exact(mode, monkeypatch):
     """Integer entries in {-4..4}: every partial sum is exact, so the split
     result equals the exact product bit for bit."""
-    import numpy as np
-
     A, B = inputs.make_integer(200, 300, 1024, seed=12)
     A, B = A.to(gu.in_dtype(mode)), B.to(gu.in_dtype(mode))
-    C = gu.run(mode, A.cuda(), B.cuda()).cpu().numpy()
     exact = A.float().numpy().astype(np.int64) @ B.float().numpy().astype(np.int64)
-    assert np.array_equal(C.astype(np.float64), exact.astype(np.float64))
+    for env in ("", "3", "8"):
+        if env:
+            monkeypatch.setenv("DGEMM_TC_SPLITK", env)
+        C = gu.run(mode, A.cuda(), B.cuda()).cpu().numpy()
+        assert np.array_equal(C.astype(np.float64), exact.astype(np.float64)), env
