@@ -248,24 +248,48 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     __syncthreads();
     if (!last) return;
     __threadfence();
+    // Sum the parts in part order and write C.  The accumulators are dead
+    // here, so the tile is walked as a flat array of float4s (consecutive
+    // threads, consecutive columns): a batch of CH float4s per thread is
+    // loaded from one part at a time, all in flight together, so each part
+    // costs one L2 round trip per batch.  -0 + x is x exactly, so the first
+    // add copies part 0.
     const float *parts0 = work + slot * (BM * BN);
+    constexpr int Q = BN / 4;                         // float4s per tile row
+    constexpr int V = BM * Q / G::THREADS;            // float4s per thread
+    constexpr int CH = 16;
+    static_assert(V % CH == 0, "whole batches");
+#pragma unroll 1
+    for (int c0 = 0; c0 < V; c0 += CH) {
+      float4 sum[CH];
 #pragma unroll
-    for (int i = 0; i < TM; ++i) {
-      const int rl = row_base + (i / 4) * G::LM * 4 + (i % 4);
+      for (int q = 0; q < CH; ++q) sum[q] = make_float4(-0.f, -0.f, -0.f, -0.f);
+      for (int p = 0; p < split_parts; ++p) {
+        const float4 *src = reinterpret_cast<const float4 *>(parts0 + (int64_t)p * (BM * BN));
 #pragma unroll
-      for (int h = 0; h < TN / 4; ++h) {
-        const int cl = col_base + h * G::LN * 4;
-        float4 sum = __ldcg(reinterpret_cast<const float4 *>(parts0 + rl * BN + cl));
-        for (int p = 1; p < split_parts; ++p) {
-          const float4 v =
-              __ldcg(reinterpret_cast<const float4 *>(parts0 + p * (BM * BN) + rl * BN + cl));
-          sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
+        for (int q = 0; q < CH; ++q) {
+          const float4 v = __ldcg(src + (c0 + q) * G::THREADS + tid);
+          sum[q].x += v.x, sum[q].y += v.y, sum[q].z += v.z, sum[q].w += v.w;
         }
-        acc[i][h * 4] = sum.x, acc[i][h * 4 + 1] = sum.y;
-        acc[i][h * 4 + 2] = sum.z, acc[i][h * 4 + 3] = sum.w;
+      }
+#pragma unroll
+      for (int q = 0; q < CH; ++q) {
+        const int e = (c0 + q) * G::THREADS + tid;
+        const int r = m0 + e / Q, c = n0 + (e % Q) * 4;
+        if (r >= M) continue;
+        float *d = C + (int64_t)r * ldc + c;
+        if (c_vec && c + 3 < N) {
+          *reinterpret_cast<float4 *>(d) = sum[q];
+        } else {
+          if (c < N) d[0] = sum[q].x;
+          if (c + 1 < N) d[1] = sum[q].y;
+          if (c + 2 < N) d[2] = sum[q].z;
+          if (c + 3 < N) d[3] = sum[q].w;
+        }
       }
     }
     if (threadIdx.x == 0) counters[tile - split_first] = 0u;
+    return;
   }
 
   // ---- epilogue: masked stores, 128-bit where C rows are 16-byte aligned
