@@ -1044,8 +1044,10 @@ int active_clusters(Kern kern, int threads, int smem, int dev, int size) {
   return n > 0 ? n : 0;
 }
 
-// Parts per tile for the single-CTA kernel.  A problem whose tiles would
-// leave more than half the SMs idle splits each tile along K into up to 8
+// Parts per tile for the single-CTA kernel.  "第八课：GPU 如何完成矩阵乘法"
+// section 十七 weighs tile size (reuse) against concurrency; here the tile
+// keeps its size and a problem whose tiles would leave more than half the
+// SMs idle gains concurrency by splitting each tile along K into up to 8
 // parts of at least 4 k-blocks (every part non-empty), the largest count whose
 // clusters are all resident at once.  DGEMM_TC_SPLITK=0 disables the split;
 // DGEMM_TC_SPLITK=2..8 forces that many parts (as far as the k-blocks allow;
