@@ -109,6 +109,16 @@ def mode_peak(mode, peaks, num_sms):
     return "tensor", bf16 * r, f"measured bf16 burst x nominal tf32/bf16 ratio {r:.4f}"
 
 
+def kernel_name(mode, M, N, num_sms):
+    """The kernel the library runs for this mode and shape: the CTA-pair
+    tensor-core kernel once there are 256 x 256 tiles for at least a quarter
+    of the SMs, else the single-CTA one (the library's own rule)."""
+    if mode == "simt":
+        return "sgemm_simt_kernel"
+    pair_tiles = ((M + 255) // 256) * ((N + 255) // 256)
+    return "tc2_gemm_kernel (CTA pair)" if pair_tiles * 4 >= num_sms else "tc_gemm_kernel"
+
+
 def source_sha(mode):
     csrc = os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc")
     files = ["simt.cu"] if mode == "simt" else ["tc.cu", "ptx.cuh"]
@@ -549,7 +559,7 @@ def run_ours(args, dist):
     achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                 "frac": achieved / peak, "traffic": profiled_traffic(mode, w.name),
-                "kernel": "tc_gemm_kernel" if mode != "simt" else "sgemm_simt_kernel",
+                "kernel": kernel_name(mode, w.M, w.N, num_sms),
                 "peak_source": f"{peak_src}: {peak_how}",
                 "per_launch_flops": w.flops, "launches_per_step": launches_per_step}
 

@@ -19,7 +19,7 @@ LIB = os.path.join(PKG, "libdgemm.so")
 HEADER = os.path.join(ROOT, "include", "dgemm.h")
 # (source, object name, defines): simt.cu and tc.cu are compiled once per
 # operand layout so that the four layouts build in parallel.
-UNITS = ([("api.cu", "api", [])]
+UNITS = ([("api.cu", "api", []), ("staging.cu", "staging", [])]
          + [("simt.cu", f"simt_{u}", [f"-DDGEMM_SIMT_UNIT={u}"]) for u in range(4)]
          + [("tc.cu", f"tc_{u}", [f"-DDGEMM_TC_UNIT={u}"]) for u in range(4)])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -12,7 +12,8 @@
 // Shipped shape (chosen by measurement on GB300 over tile shapes, BK, lane
 // orders, unroll depths and packed fma.rn.f32x2 variants): block tile
 // 128 x 256 x 16, 256 threads as 2 x 4 warps of 64 x 64, lanes 8 x 4, an
-// 8 x 16 register tile per thread, one CTA per SM (about 250 registers).
+// 8 x 16 register tile per thread, one CTA per SM, the inner product in
+// packed two-wide FMAs (DGEMM_SIMT_FFMA2).
 // GB300 specifics that differ from the pages' kernels:
 //  * A is stored transposed (k-major) in shared memory so that both operand
 //    fragments are read with 128-bit shared loads; its rows carry a 4-float
@@ -32,6 +33,15 @@
 // parallel.  Unit 0 also holds the dispatch and the zero fill.
 #ifndef DGEMM_SIMT_UNIT
 #define DGEMM_SIMT_UNIT 0
+#endif
+// 1 (default): the inner product issues the packed two-wide fma.rn.f32x2,
+// one instruction per two multiply-adds of a row of the register tile; 0:
+// scalar fmaf.  Both round each multiply-add once, in the same order, so they
+// give bitwise identical C.  The kernel is bound by instruction issue (about
+// 12% of its instructions are not FFMAs), and halving the FFMA instructions
+// measured 52.7 -> 59.8 TFLOP/s at 8192^3 on GB300.
+#ifndef DGEMM_SIMT_FFMA2
+#define DGEMM_SIMT_FFMA2 1
 #endif
 #define DG_SCAT2(a, b) a##b
 #define DG_SCAT(a, b) DG_SCAT2(a, b)
@@ -135,11 +145,21 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   const int row_base = wm * (BM / G::WM) + lm * 4;   // + c * LM * 4, c < TM / 4
   const int col_base = wn * (BN / G::WN) + ln * 4;   // + c * LN * 4, c < TN / 4
 
+#if DGEMM_SIMT_FFMA2
+  // Packed accumulators: acc2[i][h] = {acc[i][2h], acc[i][2h+1]} for the
+  // two-wide fma.rn.f32x2 (one instruction per two multiply-adds).
+  uint64_t acc2[TM][TN / 2];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int h = 0; h < TN / 2; ++h) acc2[i][h] = 0ull;  // two +0.0f
+#else
   float acc[TM][TN];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+#endif
 
   // global -> shared assignment, 128-bit vectors along each stored row:
   // A: BM rows x BK/4 (stored M x K) or BK rows x BM/4 (stored K x M);
@@ -215,14 +235,39 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
             *reinterpret_cast<const float4 *>(&Bs[cur][kk][col_base + c * G::LN * 4]);
         b[4 * c] = v.x, b[4 * c + 1] = v.y, b[4 * c + 2] = v.z, b[4 * c + 3] = v.w;
       }
+#if DGEMM_SIMT_FFMA2
+      // {a_i, a_i} x {b_2h, b_2h+1} + acc2[i][h]: a_i duplicated into a
+      // register pair (one move per row), b pairs straight from the 128-bit
+      // shared loads.
+#pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        uint64_t aa;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(aa) : "f"(a[i]));
+#pragma unroll
+        for (int h = 0; h < TN / 2; ++h) {
+          uint64_t bb;
+          asm("mov.b64 %0, {%1, %2};" : "=l"(bb) : "f"(b[2 * h]), "f"(b[2 * h + 1]));
+          asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i][h]) : "l"(aa), "l"(bb));
+        }
+      }
+#else
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+#endif
     }
     if (more) store_tiles(cur ^ 1);
     __syncthreads();
   }
+#if DGEMM_SIMT_FFMA2
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int h = 0; h < TN / 2; ++h)
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[i][2 * h]), "=f"(acc[i][2 * h + 1]) : "l"(acc2[i][h]));
+#endif
 
   if (split) {
     // Park this part's partial tile; the last part to finish sums all parts
@@ -381,7 +426,11 @@ __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ld
 }  // namespace
 
 // The configuration the library ships (see the variant table in the design doc).
-using SimtShipped = SimtCfg<128, 256, 16, 2, 4, 8, 1>;
+// (DGEMM_SIMT_CFG overrides it for tuning sweeps: BM,BN,BK,WM,WN,LM,MIN_BLOCKS.)
+#ifndef DGEMM_SIMT_CFG
+#define DGEMM_SIMT_CFG 128, 256, 16, 2, 4, 8, 1
+#endif
+using SimtShipped = SimtCfg<DGEMM_SIMT_CFG>;
 
 // This unit's operand layout.
 cudaError_t DG_SIMT_UNIT_LAUNCHER(int M, int N, int K, const float *A, int64_t lda,

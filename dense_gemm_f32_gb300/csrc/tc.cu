@@ -43,7 +43,7 @@
 // This file is compiled once per operand layout: DGEMM_TC_UNIT = 2 * AT + BT
 // selects which kernels one translation unit instantiates (AT: A stored
 // K x M; BT: B stored N x K), so the four layouts compile in parallel.  Unit
-// 0 also holds the watchdog word, the re-pitch kernel and the dispatch.
+// 0 also holds the watchdog word and the dispatch.
 #ifndef DGEMM_TC_UNIT
 #define DGEMM_TC_UNIT 0
 #endif
@@ -1195,26 +1195,6 @@ cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const v
 }
 
 #if DGEMM_TC_UNIT == 0
-__global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_bytes,
-                               uint8_t *__restrict__ dst, int64_t ldd_bytes, int rows,
-                               int64_t row_bytes, int64_t pad_bytes, int es) {
-  // one element per thread-iteration; the padding columns are zeroed
-  const int64_t per_row = (row_bytes + pad_bytes) / es;
-  const int64_t total = (int64_t)rows * per_row;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / per_row, c = (e - r * per_row) * es;
-    uint8_t *d = dst + r * ldd_bytes + c;
-    if (es == 4) {
-      *reinterpret_cast<uint32_t *>(d) =
-          c < row_bytes ? *reinterpret_cast<const uint32_t *>(src + r * lds_bytes + c) : 0u;
-    } else {
-      *reinterpret_cast<uint16_t *>(d) =
-          c < row_bytes ? *reinterpret_cast<const uint16_t *>(src + r * lds_bytes + c) : 0;
-    }
-  }
-}
-
 __global__ void read_watchdog_kernel(int *out) {
   *out = g_watchdog;
   g_watchdog = 0;
@@ -1276,21 +1256,6 @@ cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, cons
     default:
       return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
   }
-}
-
-cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
-                           int cols, int elem_bytes, int num_sms, cudaStream_t stream) {
-  const int64_t total = (int64_t)rows * ldd;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
-  if (blocks < 1) blocks = 1;
-  repitch_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      static_cast<const uint8_t *>(src), lds * elem_bytes, static_cast<uint8_t *>(dst),
-      ldd * elem_bytes, rows, (int64_t)cols * elem_bytes, (ldd - cols) * (int64_t)elem_bytes,
-      elem_bytes);
-  const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) count_launch();
-  return e;
 }
 
 cudaError_t read_watchdog(cudaStream_t stream, int *code) {
