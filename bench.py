@@ -5,14 +5,14 @@ One step is one call of the library's C entry point on one batch of
 synthetic input resident in HBM (dispatch, optional re-pitch, the GEMM
 kernel with its loads, MMAs and epilogue).  The headline line times the
 TF32 tensor-core path at M = N = K = 8192; the same run also times every
-other mode (FP32 SIMT and 3xTF32 at 8192^3, BF16 and TF32 at the
-16384 x 14336 x 4096 transformer-layer shape) and reports them under
+other mode (FP32 SIMT and 3xTF32 at 8192^3; BF16, FP16, FP8 E4M3 / E5M2
+and TF32 at the 16384 x 14336 x 4096 transformer-layer shape) and reports them under
 "modes".  Inputs are larger than L2 (129 MB), so no flush is needed.  The
 small workloads (64^3, 1024^3, ragged 1000 x 1013 x 997) are timed per mode
 under "small", with L2 warm (CUDA-graph replay) and with L2 flushed before
 each call.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode tf32|3xtf32|simt|bf16]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode tf32|3xtf32|simt|bf16|fp16|e4m3|e5m2]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
 
 Multi-GPU (launched by torch.distributed.run): every rank runs its own
@@ -38,7 +38,7 @@ METRIC = "GEMM TFLOP/s (2MNK/t) at 8192³ per mode; % of FP32/TF32/BF16 dense pe
 UNIT = "TFLOP/s"
 # Nominal dense tensor rates (PFLOP/s): the ratio converts the measured BF16
 # peak into peaks for the other tensor-core types.
-NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
+NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1, "fp8": 4.5}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 
@@ -50,7 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--mode", choices=["tf32", "3xtf32", "simt", "bf16", "fp16"], default="tf32")
+    p.add_argument("--mode", choices=["tf32", "3xtf32", "simt", "bf16", "fp16", "e4m3", "e5m2"],
+                   default="tf32")
     p.add_argument("--no-modes", action="store_true", help="headline only, skip the per-mode table")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -75,12 +76,17 @@ def workload_for(mode, transformer=False, shape=None):
     if shape:
         M, N, K = (int(x) for x in shape.split(","))
         return inputs.Workload(f"uniform {M}x{N}x{K}", M, N, K, 3, "uniform", bf16=(mode == "bf16"),
-                               fp16=(mode == "fp16"))
+                               fp16=(mode == "fp16"),
+                               fp8=mode if mode in ("e4m3", "e5m2") else "")
 
     if mode == "bf16":
         return inputs.TRANSFORMER_BF16
     if mode == "fp16":
         return inputs.TRANSFORMER_F16
+    if mode == "e4m3":
+        return inputs.TRANSFORMER_E4M3
+    if mode == "e5m2":
+        return inputs.TRANSFORMER_E5M2
     return inputs.TRANSFORMER_F32 if transformer else inputs.SQUARE_8192
 
 
@@ -105,6 +111,9 @@ def mode_peak(mode, peaks, num_sms):
         return "tensor", bf16, "measured cuBLAS bf16 burst"
     if mode == "fp16":
         return "tensor", bf16, "measured cuBLAS bf16 burst (fp16 and bf16 share the nominal rate)"
+    if mode in ("e4m3", "e5m2"):
+        r = NOMINAL_PF["fp8"] / NOMINAL_PF["bf16"]
+        return "tensor", bf16 * r, f"measured bf16 burst x nominal fp8/bf16 ratio {r:.1f}"
     r = NOMINAL_PF["tf32"] / NOMINAL_PF["bf16"]
     return "tensor", bf16 * r, f"measured bf16 burst x nominal tf32/bf16 ratio {r:.4f}"
 
@@ -337,15 +346,13 @@ def run_reference(args, dist):
 
 # ----------------------------------------------------------------- GPU arm
 def device_inputs(w, mode, device):
-    import torch
-
+    import dense_gemm_f32_gb300 as dg
     from dense_gemm_f32_gb300 import inputs
 
     A, B = inputs.make(w)
-    if mode == "bf16" and not w.bf16:
-        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
-    if mode == "fp16" and not w.fp16:
-        A, B = A.to(torch.float16), B.to(torch.float16)
+    want = dg.input_dtype(mode)
+    if A.dtype != want:  # a float32 workload timed in a narrower mode
+        A, B = A.float().to(want), B.float().to(want)
     return A, B, A.to(device), B.to(device)
 
 
@@ -426,7 +433,7 @@ def time_graph(mode, Ad, Bd, C, device, calls=20, replays=5):
     return e0.elapsed_time(e1) * 1e3 / (calls * replays)
 
 
-SMALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16")
+SMALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16", "e4m3", "e5m2")
 
 
 def time_small(device, dist, steps=20):
@@ -579,7 +586,7 @@ def run_ours(args, dist):
     modes = {}
     if not args.no_modes:
         table = [("simt", False), ("tf32", False), ("3xtf32", False), ("bf16", True),
-                 ("fp16", True), ("tf32", True)]
+                 ("fp16", True), ("e4m3", True), ("e5m2", True), ("tf32", True)]
         for m, tr in table:
             wm = workload_for(m, transformer=tr)
             if m == mode and wm.name == w.name:
@@ -618,7 +625,7 @@ def run_ours(args, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": agg["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {"tf32": "tf32", "3xtf32": "3xtf32", "simt": "f32", "bf16": "bf16",
-                      "fp16": "fp16"}[mode],
+                      "fp16": "fp16", "e4m3": "fp8-e4m3", "e5m2": "fp8-e5m2"}[mode],
             "data": "synthetic (seeded, shapes and distributions of the workload)",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "mode": mode,
                        "layout": f"row-major, compact leading dimensions, op(A) op(B) = "

@@ -11,15 +11,15 @@ libdgemm.so every call raises.
 """
 from ._lib import (  # noqa: F401  (re-exported C entry points)
     ERR_ALIAS, ERR_ARCH, ERR_CUDA, ERR_INVALID_POINTER, ERR_INVALID_VALUE, ERR_MISALIGNED,
-    ERR_NULL_POINTER, ERR_SCRATCH_LIMIT, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, LIB_PATH,
-    NOALLOC_SCRATCH_BYTES, OK, OP_N, OP_T, PATH_3XTF32, PATH_BF16, PATH_FP16, PATH_SIMT,
-    PATH_TF32, TC_3XTF32, dgemm_gemm_ex,
-    TC_TF32, LibraryMissing, dgemm_kernel_launches, dgemm_last_cuda_error, dgemm_status_string, dgemm_version,
-    dgemm_watchdog_status, gemm_bf16_tc, gemm_f16_tc, gemm_f32_simt, gemm_f32_tc,
-    gemm_f32_tc_noalloc, load,
+    ERR_NULL_POINTER, ERR_SCRATCH_LIMIT, ERR_UNSUPPORTED, ERR_WATCHDOG, EXPORTED, F8_E4M3,
+    F8_E5M2, LIB_PATH, NOALLOC_SCRATCH_BYTES, OK, OP_N, OP_T, PATH_3XTF32, PATH_BF16,
+    PATH_F8_E4M3, PATH_F8_E5M2, PATH_FP16, PATH_SIMT, PATH_TF32, TC_3XTF32, TC_TF32,
+    LibraryMissing, dgemm_gemm_ex, dgemm_kernel_launches, dgemm_last_cuda_error,
+    dgemm_status_string, dgemm_version, dgemm_watchdog_status, gemm_bf16_tc, gemm_f16_tc,
+    gemm_f32_simt, gemm_f32_tc, gemm_f32_tc_noalloc, gemm_f8_tc, load,
 )
 
-MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16")
+MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16", "e4m3", "e5m2")
 
 
 class DgemmError(RuntimeError):
@@ -49,14 +49,23 @@ def _ld(X, cols):
 
 
 _PATH = {"simt": PATH_SIMT, "tf32": PATH_TF32, "3xtf32": PATH_3XTF32, "bf16": PATH_BF16,
-         "fp16": PATH_FP16}
+         "fp16": PATH_FP16, "e4m3": PATH_F8_E4M3, "e5m2": PATH_F8_E5M2}
+
+
+def input_dtype(mode):
+    """The torch dtype of A and B for a mode."""
+    import torch
+
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "e4m3": torch.float8_e4m3fn,
+            "e5m2": torch.float8_e5m2}.get(mode, torch.float32)
 
 
 def matmul(A, B, mode="tf32", out=None, stream=None, trans_a=False, trans_b=False):
     """C = op(A) @ op(B) on the GPU through the C ABI.
 
     A, B: CUDA tensors as stored, float32 for modes simt / tf32 / 3xtf32,
-    bfloat16 for mode bf16, float16 for mode fp16; rows may be strided
+    bfloat16 for mode bf16, float16 for mode fp16, float8_e4m3fn / float8_e5m2
+    for modes e4m3 / e5m2; rows may be strided
     (leading dimension = stride(0)).  op(A) = A.T when trans_a (A stored
     K x M), else A (M x K); op(B) = B.T when trans_b (B stored N x K), else B.
     out: optional float32 (M, N) CUDA tensor view to overwrite.
@@ -66,7 +75,7 @@ def matmul(A, B, mode="tf32", out=None, stream=None, trans_a=False, trans_b=Fals
 
     if mode not in MODES:
         raise ValueError(f"mode must be one of {MODES}")
-    want = {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
+    want = input_dtype(mode)
     if A.dtype != want or B.dtype != want:
         raise TypeError(f"mode {mode} takes {want} inputs, got {A.dtype} and {B.dtype}")
     if A.dim() != 2 or B.dim() != 2:
@@ -96,7 +105,10 @@ def matmul(A, B, mode="tf32", out=None, stream=None, trans_a=False, trans_b=Fals
         st = gemm_f32_tc(TC_3XTF32, M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
     elif mode == "bf16":
         st = gemm_bf16_tc(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
-    else:
+    elif mode == "fp16":
         st = gemm_f16_tc(M, N, K, pa, lda, pb, ldb, pc, ldc, stream)
+    else:
+        st = gemm_f8_tc(F8_E4M3 if mode == "e4m3" else F8_E5M2, M, N, K, pa, lda, pb, ldb, pc,
+                        ldc, stream)
     check(st, f"gemm ({mode})")
     return out

@@ -29,11 +29,14 @@ TC_3XTF32 = 1
 
 OP_N = 0
 OP_T = 1
-PATH_SIMT, PATH_TF32, PATH_3XTF32, PATH_BF16, PATH_FP16 = range(5)
+PATH_SIMT, PATH_TF32, PATH_3XTF32, PATH_BF16, PATH_FP16, PATH_F8_E4M3, PATH_F8_E5M2 = range(7)
+F8_E4M3 = 0
+F8_E5M2 = 1
 
 EXPORTED = ("gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
             "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-            "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc", "dgemm_gemm_ex")
+            "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc", "dgemm_gemm_ex",
+            "gemm_f8_tc")
 
 _lib = None
 
@@ -77,6 +80,8 @@ def load():
     lib.gemm_f16_tc.restype = i
     lib.dgemm_gemm_ex.argtypes = [i, i, i] + gemm_args
     lib.dgemm_gemm_ex.restype = i
+    lib.gemm_f8_tc.argtypes = [i] + gemm_args
+    lib.gemm_f8_tc.restype = i
     _lib = lib
     return lib
 
@@ -101,6 +106,10 @@ def gemm_bf16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
 
 def gemm_f16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream=0):
     return load().gemm_f16_tc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f8_tc(fmt, M, N, K, A, lda, B, ldb, C, ldc, stream=0):
+    return load().gemm_f8_tc(fmt, M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def dgemm_gemm_ex(path, op_a, op_b, M, N, K, A, lda, B, ldb, C, ldc, stream=0):

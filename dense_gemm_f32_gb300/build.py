@@ -25,7 +25,8 @@ UNITS = ([("api.cu", "api", []), ("staging.cu", "staging", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 EXPORTS = ["gemm_f32_simt", "gemm_f32_tc", "gemm_bf16_tc", "dgemm_status_string",
            "dgemm_last_cuda_error", "dgemm_watchdog_status", "dgemm_version",
-           "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc", "dgemm_gemm_ex"]
+           "dgemm_kernel_launches", "gemm_f32_tc_noalloc", "gemm_f16_tc", "dgemm_gemm_ex",
+           "gemm_f8_tc"]
 
 
 def _nvcc():

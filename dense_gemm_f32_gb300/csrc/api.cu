@@ -186,11 +186,55 @@ int after_launch(cudaError_t e, const char *what) {
 // TMA needs 16-byte aligned bases and row pitches that are multiples of 16 B.
 inline bool tma_ok(const void *p, int64_t ld, int es) { return aligned(p, 16) && (ld * es) % 16 == 0; }
 
+inline bool is_f8(dg::TcKind k) { return k == dg::TcKind::kE4M3 || k == dg::TcKind::kE5M2; }
+
+int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A, int lda,
+           const void *B, int ldb, float *C, int ldc, int num_sms, cudaStream_t stream);
+
+// 8-bit operands: the tensor cores read them K-major only, so A stored K x M
+// and B stored K x N are first transposed into scratch (A as M x K, B as
+// N x K, pitch rounded up to 16 bytes); K-major operands whose rows are not
+// 16-byte aligned are re-pitched by run_tc as usual.
+int run_tc_f8(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A, int lda,
+              const void *B, int ldb, float *C, int ldc, int num_sms, cudaStream_t stream) {
+  if (!a_t && b_t)
+    return run_tc(kind, false, true, M, N, K, A, lda, B, ldb, C, ldc, num_sms, stream);
+  const int64_t kp = (K + 15) / 16 * 16;  // K-major pitch of a transposed operand
+  const size_t a_bytes = a_t ? (size_t)(((int64_t)M * kp + 255) / 256 * 256) : 0;
+  const size_t b_bytes = b_t ? 0 : (size_t)(((int64_t)N * kp + 255) / 256 * 256);
+  void *scratch = nullptr;
+  cudaError_t e = dg::scratch_alloc(&scratch, a_bytes + b_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scratch allocation (8-bit transpose)");
+  char *s = static_cast<char *>(scratch);
+  const void *Ause = A, *Buse = B;
+  int lda_use = lda, ldb_use = ldb;
+  int st = DGEMM_OK;
+  if (a_t) {  // A stored K x M -> M x K
+    e = dg::launch_transpose8(A, lda, s, kp, K, M, num_sms, stream);
+    Ause = s;
+    lda_use = (int)kp;
+  }
+  if (e == cudaSuccess && !b_t) {  // B stored K x N -> N x K
+    e = dg::launch_transpose8(B, ldb, s + a_bytes, kp, K, N, num_sms, stream);
+    Buse = s + a_bytes;
+    ldb_use = (int)kp;
+  }
+  if (e != cudaSuccess)
+    st = cuda_fail(e, "8-bit transpose launch");
+  else
+    st = run_tc(kind, false, true, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc, num_sms, stream);
+  const cudaError_t e2 = dg::scratch_free(scratch, stream);
+  if (st == DGEMM_OK && e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
+  return st;
+}
+
 // Tensor-core GEMM with operands re-pitched into stream-ordered scratch when
 // their rows do not start on 16-byte boundaries.
 int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A, int lda,
            const void *B, int ldb, float *C, int ldc, int num_sms, cudaStream_t stream) {
-  const int es = (kind == dg::TcKind::kBF16 || kind == dg::TcKind::kF16) ? 2 : 4;
+  const int es = is_f8(kind) ? 1
+                 : (kind == dg::TcKind::kBF16 || kind == dg::TcKind::kF16) ? 2
+                                                                            : 4;
   const int64_t pitch_elems = 16 / es;
   const int a_rows = a_t ? K : M, a_cols = a_t ? M : K;  // storage shapes
   const int b_rows = b_t ? N : K, b_cols = b_t ? K : N;
@@ -353,13 +397,26 @@ int gemm_f16_tc(int M, int N, int K, const unsigned short *A, int lda, const uns
   return run_tc(dg::TcKind::kF16, false, false, M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
 }
 
+int gemm_f8_tc(int format, int M, int N, int K, const unsigned char *A, int lda,
+               const unsigned char *B, int ldb, float *C, int ldc, cudaStream_t stream) {
+  if (format != DGEMM_F8_E4M3 && format != DGEMM_F8_E5M2) return DGEMM_ERR_UNSUPPORTED;
+  bool none = false;
+  int dev = 0, sms = 0;
+  int st = validate(M, N, K, false, false, A, lda, B, ldb, C, ldc, 1, &none, &dev, &sms);
+  if (st != DGEMM_OK || none) return st;
+  if (K == 0) return after_launch(dg::launch_zero_fill(C, M, N, ldc, sms, stream), "zero fill");
+  return run_tc_f8(format == DGEMM_F8_E4M3 ? dg::TcKind::kE4M3 : dg::TcKind::kE5M2, false, false,
+                   M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
+}
+
 int dgemm_gemm_ex(int path, int op_a, int op_b, int M, int N, int K, const void *A, int lda,
                   const void *B, int ldb, float *C, int ldc, cudaStream_t stream) {
-  if (path < DGEMM_PATH_SIMT || path > DGEMM_PATH_FP16) return DGEMM_ERR_UNSUPPORTED;
+  if (path < DGEMM_PATH_SIMT || path > DGEMM_PATH_F8_E5M2) return DGEMM_ERR_UNSUPPORTED;
   if ((op_a != DGEMM_OP_N && op_a != DGEMM_OP_T) || (op_b != DGEMM_OP_N && op_b != DGEMM_OP_T))
     return DGEMM_ERR_UNSUPPORTED;
   const bool a_t = op_a == DGEMM_OP_T, b_t = op_b == DGEMM_OP_T;
-  const int es = (path == DGEMM_PATH_BF16 || path == DGEMM_PATH_FP16) ? 2 : 4;
+  const bool f8 = path == DGEMM_PATH_F8_E4M3 || path == DGEMM_PATH_F8_E5M2;
+  const int es = f8 ? 1 : (path == DGEMM_PATH_BF16 || path == DGEMM_PATH_FP16) ? 2 : 4;
   bool none = false;
   int dev = 0, sms = 0;
   int st = validate(M, N, K, a_t, b_t, A, lda, B, ldb, C, ldc, es, &none, &dev, &sms);
@@ -373,6 +430,9 @@ int dgemm_gemm_ex(int path, int op_a, int op_b, int M, int N, int K, const void 
                                         c_vec, sms, stream),
                         "SIMT GEMM launch");
   }
+  if (f8)
+    return run_tc_f8(path == DGEMM_PATH_F8_E4M3 ? dg::TcKind::kE4M3 : dg::TcKind::kE5M2, a_t, b_t,
+                     M, N, K, A, lda, B, ldb, C, ldc, sms, stream);
   const dg::TcKind kind = path == DGEMM_PATH_TF32    ? dg::TcKind::kTF32
                           : path == DGEMM_PATH_3XTF32 ? dg::TcKind::k3xTF32
                           : path == DGEMM_PATH_BF16   ? dg::TcKind::kBF16

@@ -32,7 +32,7 @@ cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
                              cudaStream_t stream);
 
 // Element type of a tensor-core GEMM's operands.
-enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2, kF16 = 3 };
+enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2, kF16 = 3, kE4M3 = 4, kE5M2 = 5 };
 
 // tcgen05 GEMM, C = op(A) op(B).  a_t: A is stored K x M (op(A) = A^T), else
 // M x K; b_t: B is stored N x K (op(B) = B^T), else K x N; all row-major with
@@ -57,7 +57,13 @@ DG_DECLARE_TC_UNIT(2)
 DG_DECLARE_TC_UNIT(3)
 #undef DG_DECLARE_TC_UNIT
 
-// Copy a rows x cols matrix of elem_bytes-sized elements (4 or 2) from
+// dst = src^T for a rows x cols matrix of bytes (leading dimensions in
+// bytes): dst is cols x rows with leading dimension ldd >= rows.  Puts 8-bit
+// operands into the K-major layout (A as M x K, B as N x K).
+cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
+                              int cols, int num_sms, cudaStream_t stream);
+
+// Copy a rows x cols matrix of elem_bytes-sized elements (4, 2 or 1) from
 // (src, lds) to (dst, ldd); used to re-pitch operands whose rows do not start
 // on 16-byte boundaries.
 cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,

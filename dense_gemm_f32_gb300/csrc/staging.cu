@@ -1,5 +1,6 @@
 // staging.cu -- re-pitching of operands the tensor-memory accelerator cannot
-// address.
+// address, and the transpose of 8-bit operands into the K-major layout the
+// tensor cores read them in.
 //
 // TMA reads a matrix only if its base is 16-byte aligned and its row pitch is
 // a multiple of 16 bytes ("第八课：GPU 如何完成矩阵乘法" section 二十二 lists
@@ -31,7 +32,16 @@ __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_byte
          ch += (int64_t)gridDim.x * blockDim.x) {
       const int64_t c0 = ch * 16;
       uint32_t w[4];
-      if (es == 4) {
+      if (es == 1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (c0 + 4 * k + b < row_bytes) v |= (uint32_t)srow[c0 + 4 * k + b] << (8 * b);
+          w[k] = v;
+        }
+      } else if (es == 4) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           w[k] = c0 + 4 * k < row_bytes ? *reinterpret_cast<const uint32_t *>(srow + c0 + 4 * k)
@@ -51,7 +61,68 @@ __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_byte
   }
 }
 
+// dst = src^T for a rows x cols matrix of bytes: dst[c][r] = src[r][c].
+// 64 x 64-byte tiles, 256 threads.  Interior tiles whose rows are 4-byte
+// aligned move 32-bit words: each thread loads four words of one 4 x 4-byte
+// block through shared memory and transposes it in registers with byte
+// permutes; sixteen threads cover 64 contiguous bytes of an output row.
+// Edge tiles and unaligned operands go byte by byte.
+constexpr int kT = 64;
+__global__ void __launch_bounds__(256)
+    transpose8_kernel(const uint8_t *__restrict__ src, int64_t lds, uint8_t *__restrict__ dst,
+                      int64_t ldd, int rows, int cols, int words_ok) {
+  __shared__ uint32_t tile[kT][kT / 4 + 1];
+  const int tid = threadIdx.x;
+  const int tiles_c = (cols + kT - 1) / kT;
+  const int64_t ntiles = (int64_t)((rows + kT - 1) / kT) * tiles_c;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int r0 = (int)(t / tiles_c) * kT, c0 = (int)(t % tiles_c) * kT;
+    const bool full = words_ok && r0 + kT <= rows && c0 + kT <= cols;
+    if (full) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = tid / 16 + 16 * k, w = tid % 16;
+        tile[r][w] = *reinterpret_cast<const uint32_t *>(src + (int64_t)(r0 + r) * lds + c0 + 4 * w);
+      }
+      __syncthreads();
+      const int cb = tid / 16, rb = tid % 16;  // 4-column block, 4-row block
+      const uint32_t x0 = tile[4 * rb][cb], x1 = tile[4 * rb + 1][cb];
+      const uint32_t x2 = tile[4 * rb + 2][cb], x3 = tile[4 * rb + 3][cb];
+      const uint32_t t0 = __byte_perm(x0, x1, 0x5140), t1 = __byte_perm(x2, x3, 0x5140);
+      const uint32_t t2 = __byte_perm(x0, x1, 0x7362), t3 = __byte_perm(x2, x3, 0x7362);
+      const uint32_t o[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632),
+                             __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint32_t *>(dst + (int64_t)(c0 + 4 * cb + j) * ldd + r0 + 4 * rb) = o[j];
+      __syncthreads();
+    } else {
+      for (int e = tid; e < kT * kT; e += blockDim.x) {
+        const int i = e / kT, j = e % kT;  // output row c0 + i, output column r0 + j
+        if (c0 + i < cols && r0 + j < rows)
+          dst[(int64_t)(c0 + i) * ldd + r0 + j] = src[(int64_t)(r0 + j) * lds + c0 + i];
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
+                              int cols, int num_sms, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int64_t ntiles = (int64_t)((rows + kT - 1) / kT) * ((cols + kT - 1) / kT);
+  int64_t grid = (int64_t)num_sms * 8;
+  if (grid > ntiles) grid = ntiles;
+  const bool words_ok = reinterpret_cast<uintptr_t>(src) % 4 == 0 && lds % 4 == 0 &&
+                        reinterpret_cast<uintptr_t>(dst) % 4 == 0 && ldd % 4 == 0;
+  transpose8_kernel<<<(unsigned)grid, 256, 0, stream>>>(
+      static_cast<const uint8_t *>(src), lds, static_cast<uint8_t *>(dst), ldd, rows, cols,
+      words_ok ? 1 : 0);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
 
 cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
                            int cols, int elem_bytes, int num_sms, cudaStream_t stream) {

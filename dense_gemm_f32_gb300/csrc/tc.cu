@@ -85,11 +85,18 @@ struct Cfg {
   static constexpr bool AT = AT_, BT = BT_;
   // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
   static constexpr bool k16 = KIND == TcKind::kBF16 || KIND == TcKind::kF16;
+  // 8-bit float operands (tcgen05 kind::f8f6f4), read K-major only
+  static constexpr bool k8 = KIND == TcKind::kE4M3 || KIND == TcKind::kE5M2;
   // operand format code of the instruction descriptor: F16 0, BF16 1, TF32 2
-  static constexpr uint32_t kFmt = KIND == TcKind::kF16 ? 0u : KIND == TcKind::kBF16 ? 1u : 2u;
+  // (kind::f8f6f4 codes: E4M3 0, E5M2 1)
+  static constexpr uint32_t kFmt = KIND == TcKind::kF16    ? 0u
+                                   : KIND == TcKind::kBF16 ? 1u
+                                   : KIND == TcKind::kE4M3 ? 0u
+                                   : KIND == TcKind::kE5M2 ? 1u
+                                                           : 2u;
   static constexpr bool kSplit = KIND == TcKind::k3xTF32;
   static constexpr int BN = BN_;
-  static constexpr int ES = k16 ? 2 : 4;        // operand element bytes
+  static constexpr int ES = k8 ? 1 : k16 ? 2 : 4;  // operand element bytes
   static constexpr int BK = 128 / ES;             // k per stage: one 128-B swizzle row
   static constexpr int UMMA_K = 32 / ES;          // k per MMA instruction (32 bytes)
   static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per stage (per product)
@@ -138,6 +145,7 @@ struct Cfg {
   // 32-byte atoms for 32-bit ones (layout type 1); K-group stride 1024 / 512 B.
   static constexpr uint32_t MN_LAYOUT = k16 ? 2u : 1u;
   static constexpr uint32_t MN_SBO = k16 ? 1024u : 512u;
+  static_assert(!k8 || (!AT && BT), "8-bit operands are read K-major: A as M x K, B as N x K");
 
   // Instruction descriptor: D fp32, A/B format, A major (bit 15: 1 = MN),
   // B major (bit 16: 1 = MN), N >> 3 at bit 17, M >> 4 at bit 24.
@@ -363,6 +371,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
               umma_tf32(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32(d_tmem, ad, bdl, G::IDESC, 1u);      // A_hi B_lo
               umma_tf32(d_tmem, ad, bd, G::IDESC, 1u);       // A_hi B_hi
+            } else if constexpr (G::k8) {
+              umma_f8(d_tmem, ad, bd, G::IDESC, accum);
             } else if constexpr (G::k16) {
               umma_f16(d_tmem, ad, bd, G::IDESC, accum);
             } else {
@@ -568,12 +578,19 @@ struct Cfg2 {
   static constexpr bool AT = AT_, BT = BT_;
   // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
   static constexpr bool k16 = KIND == TcKind::kBF16 || KIND == TcKind::kF16;
+  // 8-bit float operands (tcgen05 kind::f8f6f4), read K-major only
+  static constexpr bool k8 = KIND == TcKind::kE4M3 || KIND == TcKind::kE5M2;
   // operand format code of the instruction descriptor: F16 0, BF16 1, TF32 2
-  static constexpr uint32_t kFmt = KIND == TcKind::kF16 ? 0u : KIND == TcKind::kBF16 ? 1u : 2u;
+  // (kind::f8f6f4 codes: E4M3 0, E5M2 1)
+  static constexpr uint32_t kFmt = KIND == TcKind::kF16    ? 0u
+                                   : KIND == TcKind::kBF16 ? 1u
+                                   : KIND == TcKind::kE4M3 ? 0u
+                                   : KIND == TcKind::kE5M2 ? 1u
+                                                           : 2u;
   static constexpr bool kSplit = KIND == TcKind::k3xTF32;
   static constexpr int BM = 256, BN = 256;           // pair tile
   static constexpr int HM = 128, HN = 128;           // per-CTA halves
-  static constexpr int ES = k16 ? 2 : 4;
+  static constexpr int ES = k8 ? 1 : k16 ? 2 : 4;
   static constexpr int BK = 128 / ES;
   static constexpr int UMMA_K = 32 / ES;
   static constexpr int KSTEPS = BK / UMMA_K;
@@ -602,6 +619,7 @@ struct Cfg2 {
   static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
   static constexpr uint32_t MN_LAYOUT = k16 ? 2u : 1u;
   static constexpr uint32_t MN_SBO = k16 ? 1024u : 512u;
+  static_assert(!k8 || (!AT && BT), "8-bit operands are read K-major: A as M x K, B as N x K");
   static constexpr uint32_t IDESC = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
                                     ((AT ? 1u : 0u) << 15) | ((BT ? 0u : 1u) << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
@@ -786,6 +804,8 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
               umma_tf32_pair(d_tmem, adl, bd, G::IDESC, accum);  // A_lo B_hi
               umma_tf32_pair(d_tmem, ad, bdl, G::IDESC, 1u);     // A_hi B_lo
               umma_tf32_pair(d_tmem, ad, bd, G::IDESC, 1u);      // A_hi B_hi
+            } else if constexpr (G::k8) {
+              umma_f8_pair(d_tmem, ad, bd, G::IDESC, accum);
             } else if constexpr (G::k16) {
               umma_f16_pair(d_tmem, ad, bd, G::IDESC, accum);
             } else {
@@ -993,6 +1013,7 @@ template <TcKind KIND>
 constexpr CUtensorMapDataType tma_type() {
   return KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
          : KIND == TcKind::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+         : (KIND == TcKind::kE4M3 || KIND == TcKind::kE5M2) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 }
 
@@ -1006,7 +1027,7 @@ bool make_operand_maps(CUtensorMap *ta, CUtensorMap *tb, int M, int N, int K, co
                        int64_t lda, const void *B, int64_t ldb, int rows_a, int cols_b) {
   const CUtensorMapDataType dt = tma_type<KIND>();
   const CUtensorMapSwizzle mn_swz =
-      G::k16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+      (G::k16 || G::k8) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
   const bool ok_a = G::AT ? make_map(ta, A, dt, G::ES, K, M, lda, G::BOX, G::BK, mn_swz)
                           : make_map(ta, A, dt, G::ES, M, K, lda, G::BK, rows_a,
                                      CU_TENSOR_MAP_SWIZZLE_128B);
@@ -1220,6 +1241,17 @@ cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, in
     case TcKind::kF16:
       return launch_kind<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                             watchdog, stream);
+    case TcKind::kE4M3:
+    case TcKind::kE5M2:
+      // 8-bit operands exist only K-major (A as M x K, B as N x K): this unit
+      if constexpr (!kUnitAT && kUnitBT) {
+        if (kind == TcKind::kE4M3)
+          return launch_kind<TcKind::kE4M3, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
+                                                 num_sms, watchdog, stream);
+        return launch_kind<TcKind::kE5M2, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                               watchdog, stream);
+      }
+      return cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }

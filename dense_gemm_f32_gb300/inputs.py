@@ -13,9 +13,9 @@ Recipe (the pages fix no distribution or generator, so these are chosen):
   * normal N(0, s^2)    -> s * torch.randn(shape)
   * integer copy        -> torch.randint(-4, 5, shape) from a fresh generator
                            with the same seed, stored as float32
-  * bf16 / fp16 inputs  -> the fp32 draws rounded once to bfloat16 or float16
-                           (round to nearest even); the rounded values ARE the
-                           inputs.
+  * bf16 / fp16 / fp8   -> the fp32 draws rounded once to bfloat16, float16,
+                           float8 e4m3 or e5m2 (round to nearest even, no
+                           scaling); the rounded values ARE the inputs.
 Shapes follow the pages' workloads: the 1024 x 1024 benchmark of
 "4. 矩阵乘法（GEMM）优化" section 4.4, the M = 1000 ragged edge of Lesson 8
 section 二十六, the K = 64 = 4 x 16 tile example of Lesson 8 section 九.
@@ -37,6 +37,7 @@ class Workload:
     b_std: float = 1.0
     bf16: bool = False  # inputs rounded to bfloat16
     fp16: bool = False  # inputs rounded to float16
+    fp8: str = ""       # "e4m3" / "e5m2": inputs rounded to that 8-bit float
 
     @property
     def flops(self):
@@ -54,9 +55,15 @@ TRANSFORMER_F32 = Workload("transformer-layer 16384x14336x4096 fp32", 16384, 143
                            "normal", a_std=1.0, b_std=0.02, bf16=False)
 TRANSFORMER_F16 = Workload("transformer-layer 16384x14336x4096 fp16", 16384, 14336, 4096, 4,
                            "normal", a_std=1.0, b_std=0.02, fp16=True)
+TRANSFORMER_E4M3 = Workload("transformer-layer 16384x14336x4096 e4m3", 16384, 14336, 4096, 4,
+                            "normal", a_std=1.0, b_std=0.02, fp8="e4m3")
+TRANSFORMER_E5M2 = Workload("transformer-layer 16384x14336x4096 e5m2", 16384, 14336, 4096, 4,
+                            "normal", a_std=1.0, b_std=0.02, fp8="e5m2")
 
 ALL = [SQUARE_64, SQUARE_1024, RAGGED_1000, SQUARE_8192, TRANSFORMER_BF16, TRANSFORMER_F32,
-       TRANSFORMER_F16]
+       TRANSFORMER_F16, TRANSFORMER_E4M3, TRANSFORMER_E5M2]
+
+F8_DTYPES = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 def _draw(gen, shape, dist, std):
@@ -68,7 +75,7 @@ def _draw(gen, shape, dist, std):
 
 
 def make(w: Workload):
-    """(A, B) as CPU tensors: float32, or bfloat16 / float16 when w.bf16 / w.fp16."""
+    """(A, B) as CPU tensors: float32, or bfloat16 / float16 / float8 per w."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
     A = _draw(g, (w.M, w.K), w.dist, w.a_std)
@@ -77,6 +84,8 @@ def make(w: Workload):
         A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
     elif w.fp16:
         A, B = A.to(torch.float16), B.to(torch.float16)
+    elif w.fp8:
+        A, B = A.to(F8_DTYPES[w.fp8]), B.to(F8_DTYPES[w.fp8])
     return A, B
 
 
@@ -95,7 +104,7 @@ def make_random(M, N, K, seed, dist="uniform", dtype=torch.float32):
     g.manual_seed(seed)
     A = _draw(g, (M, K), dist, 1.0)
     B = _draw(g, (K, N), dist, 1.0)
-    if dtype in (torch.bfloat16, torch.float16):
+    if dtype in (torch.bfloat16, torch.float16, torch.float8_e4m3fn, torch.float8_e5m2):
         A, B = A.to(dtype), B.to(dtype)
     return A, B
 

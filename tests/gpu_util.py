@@ -5,20 +5,30 @@ import torch
 import oracle
 
 # |C - C_exact| <= tol * S elementwise, S = |A| x |B|; one tolerance per mode.
-# fp16: the inputs are exact, only the fp32 accumulation rounds (at most K/16
-# rounded accumulator additions of 2^-23 each: 1.2e-4 at K = 16384).
-TOL = {"simt": 1e-5, "3xtf32": 1e-5, "tf32": 2e-3, "bf16": 8e-3, "fp16": 2e-4}
+# fp16 and fp8: the inputs are exact and so are their products in fp32; only
+# the fp32 accumulation rounds (once per MMA instruction, K/16 or K/32 times:
+# below 6e-5 at K = 16384), plus the rounding inside one instruction's sum.
+TOL = {"simt": 1e-5, "3xtf32": 1e-5, "tf32": 2e-3, "bf16": 8e-3, "fp16": 2e-4,
+       "e4m3": 2e-4, "e5m2": 2e-4}
 FP32_MODES = ("simt", "tf32", "3xtf32")
 HALF_MODES = ("bf16", "fp16")
-ALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16")
+F8_MODES = ("e4m3", "e5m2")
+LOW_MODES = HALF_MODES + F8_MODES  # inputs narrower than fp32
+ALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16", "e4m3", "e5m2")
+TC_MODES = ("tf32", "3xtf32", "bf16", "fp16", "e4m3", "e5m2")
 
 
 def in_dtype(mode):
-    return {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "e4m3": torch.float8_e4m3fn,
+            "e5m2": torch.float8_e5m2}.get(mode, torch.float32)
+
+
+def elem_bytes(mode):
+    return 1 if mode in F8_MODES else 2 if mode in HALF_MODES else 4
 
 
 def np_inputs(A, B):
-    """float32 numpy copies of CPU tensors (bf16 widens exactly)."""
+    """float32 numpy copies of CPU tensors (bf16, fp16 and fp8 widen exactly)."""
     return A.float().numpy(), B.float().numpy()
 
 

@@ -153,11 +153,26 @@ def test_gemm_ex_leading_dimensions_follow_the_stored_shape(lib, path):
 
 
 def test_gemm_ex_rejects_unknown_path_or_op(lib):
-    assert dg.dgemm_gemm_ex(5, 0, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.dgemm_gemm_ex(7, 0, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
     assert dg.dgemm_gemm_ex(-1, 0, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
     assert dg.dgemm_gemm_ex(1, 2, 0, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
     assert dg.dgemm_gemm_ex(1, 0, -1, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
     assert dg.dgemm_gemm_ex(1, 0, 1, 0, 4, 4, 0, 4, 0, 4, 0, 4, 0) == dg.OK
+
+
+def test_f8_rejects_unknown_format_and_checks_arguments(lib):
+    """gemm_f8_tc: unknown format first, then the common checks (element
+    alignment is one byte, so any address is aligned)."""
+    assert dg.gemm_f8_tc(2, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.gemm_f8_tc(-1, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert dg.gemm_f8_tc(dg.F8_E4M3, 4, 4, 4, P, 3, P * 2, 4, P * 4, 4, 0) == dg.ERR_INVALID_VALUE
+    assert dg.gemm_f8_tc(dg.F8_E5M2, 4, 4, 4, 0, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_NULL_POINTER
+    assert dg.gemm_f8_tc(dg.F8_E4M3, 0, 4, 4, 0, 4, 0, 4, 0, 4, 0) == dg.OK
+    # C overlapping B
+    assert dg.gemm_f8_tc(dg.F8_E4M3, 4, 4, 4, P + 1, 4, P * 2 + 1, 4, P * 2 + 4, 4, 0) == dg.ERR_ALIAS
+    # the FP8 paths of dgemm_gemm_ex validate the transposed storage shapes
+    assert dg.dgemm_gemm_ex(dg.PATH_F8_E4M3, dg.OP_T, dg.OP_N, 4, 8, 2, P, 3, P * 2, 8,
+                            P * 4, 8, 0) == dg.ERR_INVALID_VALUE
 
 
 def test_matmul_transposed_shape_checks_need_no_gpu():

@@ -30,7 +30,7 @@ def _built():
 
 def _full_case(w, mode):
     A, B = inputs.make(w)
-    if mode in gu.HALF_MODES and A.dtype != gu.in_dtype(mode):
+    if mode in gu.LOW_MODES and A.dtype != gu.in_dtype(mode):
         A, B = A.float().to(gu.in_dtype(mode)), B.float().to(gu.in_dtype(mode))
     C = gu.run(mode, A.cuda(), B.cuda())
     ref, S = gu.oracle_full(A, B)
@@ -80,7 +80,7 @@ def test_ragged_1000x1013x997(mode):
 
 def _sampled(w, mode, nrows=48):
     A, B = inputs.make(w)
-    if mode in gu.HALF_MODES and A.dtype != gu.in_dtype(mode):
+    if mode in gu.LOW_MODES and A.dtype != gu.in_dtype(mode):
         A, B = A.float().to(gu.in_dtype(mode)), B.float().to(gu.in_dtype(mode))
     C = gu.run(mode, A.cuda(), B.cuda())
     g = np.random.default_rng(w.seed)
@@ -108,3 +108,11 @@ def test_transformer_tf32_sampled_rows():
 def test_transformer_fp16_sampled_rows():
     """The transformer-layer draws rounded to fp16 instead of bf16."""
     _sampled(inputs.TRANSFORMER_F16, "fp16", nrows=24)
+
+
+@pytest.mark.parametrize("mode", ["e4m3", "e5m2"])
+def test_transformer_fp8_sampled_rows(mode):
+    """The transformer-layer draws rounded to FP8 (scale 1), through the
+    default row-major B (transposed into K-major scratch first)."""
+    _sampled(inputs.TRANSFORMER_E4M3 if mode == "e4m3" else inputs.TRANSFORMER_E5M2, mode,
+             nrows=24)

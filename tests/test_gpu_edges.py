@@ -98,10 +98,11 @@ def test_leading_dimensions_and_guard_bands(mode):
 
 @pytest.mark.parametrize("mode", gu.ALL_MODES)
 def test_misaligned_bases(mode):
-    """Base pointers 1..3 elements past a 16-byte boundary (fp32) or 1..7
-    (bf16): not 16-byte aligned, so no 128-bit or TMA access may start there."""
+    """Base pointers 1..3 elements past a 16-byte boundary (fp32), 1..7 (16-bit)
+    or 1..15 (8-bit): not 16-byte aligned, so no 128-bit or TMA access may
+    start there."""
     M, N, K = 190, 150, 90
-    es = 2 if mode in gu.HALF_MODES else 4
+    es = gu.elem_bytes(mode)
     A, B = inputs.make_random(M, N, K, seed=37, dtype=gu.in_dtype(mode))
     for off in range(1, 16 // es):
         Ad = gu.device_view(*inputs.embed(A, K, offset=off))
@@ -133,7 +134,10 @@ def test_host_pointers_rejected(mode):
             "3xtf32": lambda a, b, c: dg.gemm_f32_tc(dg.TC_3XTF32, 64, 64, 64, a, 64, b, 64, c,
                                                      64, 0),
             "bf16": lambda a, b, c: dg.gemm_bf16_tc(64, 64, 64, a, 64, b, 64, c, 64, 0),
-            "fp16": lambda a, b, c: dg.gemm_f16_tc(64, 64, 64, a, 64, b, 64, c, 64, 0)}[mode]
+            "fp16": lambda a, b, c: dg.gemm_f16_tc(64, 64, 64, a, 64, b, 64, c, 64, 0),
+            "e4m3": lambda a, b, c: dg.gemm_f8_tc(dg.F8_E4M3, 64, 64, 64, a, 64, b, 64, c, 64, 0),
+            "e5m2": lambda a, b, c: dg.gemm_f8_tc(dg.F8_E5M2, 64, 64, 64, a, 64, b, 64, c, 64,
+                                                  0)}[mode]
     Ad, Bd = A.cuda(), B.cuda()
     assert call(A.data_ptr(), Bd.data_ptr(), C.data_ptr()) == dg.ERR_INVALID_POINTER
     Bp = B.pin_memory()

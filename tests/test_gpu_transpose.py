@@ -2,7 +2,7 @@
 
 A transposed A is stored K x M and a transposed B is stored N x K, both
 row-major (Lesson 8 section 二十八: a column-major matrix is a row-major
-transpose).  Every path (SIMT, TF32, 3xTF32, BF16, FP16) and, for the tensor
+transpose).  Every path (SIMT, TF32, 3xTF32, BF16, FP16, FP8) and, for the tensor
 cores, both kernels (single CTA and CTA pair, forced with DGEMM_TC_PAIR) are
 compared with the CPU oracle on op(A) and op(B), at the same tolerances as
 the plain product, over ragged shapes, padded leading dimensions,
