@@ -62,6 +62,10 @@ __device__ int g_watchdog = 0;
 namespace {
 
 constexpr bool kUnitAT = (DGEMM_TC_UNIT >> 1) & 1;
+// Bits of the kernels' `mn3d` argument: that MN-major operand is read through
+// a 3-D tensor map, one TMA instruction per stage (else one per 128-byte
+// column block; see make_map3).
+constexpr int kA3d = 1, kB3d = 2;
 constexpr bool kUnitBT = DGEMM_TC_UNIT & 1;
 
 constexpr int BM = 128;
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
                    int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
-                   int splits) {
+                   int splits, int mn3d) {
   using G = Cfg<KIND, BN, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -297,21 +301,29 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
+          if (AT && (mn3d & kA3d)) {  // A stored K x M, all its column blocks at once
+            tma_load_3d(a_tile(stage), &tmap_a, full_bar(stage), 0, kb * G::BK, tm * BM / G::BOX);
+          } else {
 #pragma unroll
-          for (int j = 0; j < G::A_BOXES; ++j) {
-            if constexpr (AT)  // A stored K x M: boxes of BOX columns of M x BK rows
-              tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage),
-                          tm * BM + j * G::BOX, kb * G::BK);
-            else
-              tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, tm * BM);
+            for (int j = 0; j < G::A_BOXES; ++j) {
+              if constexpr (AT)  // A stored K x M: boxes of BOX columns of M x BK rows
+                tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage),
+                            tm * BM + j * G::BOX, kb * G::BK);
+              else
+                tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, tm * BM);
+            }
           }
+          if (!BT && (mn3d & kB3d)) {  // B stored K x N, all its column blocks at once
+            tma_load_3d(b_tile(stage), &tmap_b, full_bar(stage), 0, kb * G::BK, tn * BN / G::BOX_N);
+          } else {
 #pragma unroll
-          for (int j = 0; j < G::B_BOXES; ++j) {
-            if constexpr (BT)  // B stored N x K: one box of BK x BN
-              tma_load_2d(b_tile(stage), &tmap_b, full_bar(stage), kb * G::BK, tn * BN);
-            else
-              tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
-                          tn * BN + j * G::BOX_N, kb * G::BK);
+            for (int j = 0; j < G::B_BOXES; ++j) {
+              if constexpr (BT)  // B stored N x K: one box of BK x BN
+                tma_load_2d(b_tile(stage), &tmap_b, full_bar(stage), kb * G::BK, tn * BN);
+              else
+                tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
+                            tn * BN + j * G::BOX_N, kb * G::BK);
+            }
           }
           ++issued;
           if (++stage == G::STAGES) {
@@ -607,8 +619,12 @@ struct Cfg2 {
   static constexpr int STAGES = 196608 / STAGE_BYTES;
   static constexpr int TMEM_COLS = 512;                   // two 256-column accumulators
   static constexpr int kEpiWarps = 4;
-  static constexpr int kSplitWarp0 = 6, kSplitWarps = kSplit ? 8 : 0;
-  static constexpr int THREADS = 32 * (2 + kEpiWarps + kSplitWarps);
+  // Two producer threads, one per operand, in warps 0 and kProdBWarp: a TMA
+  // instruction takes ~70 cycles to issue whatever its box size, and one
+  // thread issuing every box of a stage fell behind the MMAs.
+  static constexpr int kProdBWarp = 2 + kEpiWarps;
+  static constexpr int kSplitWarp0 = kProdBWarp + 1, kSplitWarps = kSplit ? 8 : 0;
+  static constexpr int THREADS = 32 * (3 + kEpiWarps + kSplitWarps);
   // full, empty, ready (3xTF32), accf[2], acce[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   // epilogue staging: per epilogue warp two 32 x 32 fp32 chunks (TMA stores)
@@ -624,7 +640,7 @@ struct Cfg2 {
                                     ((AT ? 1u : 0u) << 15) | ((BT ? 0u : 1u) << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
-  static_assert(kSplitWarp0 == 2 + kEpiWarps, "split warps follow the epilogue warps");
+  static_assert(kSplitWarp0 == 3 + kEpiWarps, "split warps follow the B producer warp");
 };
 
 enum : int {
@@ -643,7 +659,8 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_c, float *__restrict__ C, int M,
-                    int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog) {
+                    int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog,
+                    int mn3d) {
   using G = Cfg2<KIND, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -677,7 +694,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 2);  // one arrival per producer thread
       mbar_init(empty_bar(s), 1);
       mbar_init(ready_bar(s), G::kSplit ? 2 * G::kSplitWarps : 1);
     }
@@ -705,49 +722,64 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == G::kProdBWarp) {
+    // ----------------------------------------------------------- producers
+    // warp 0 loads this CTA's part of op(A), warp kProdBWarp its part of
+    // op(B); each arrives once per stage on the full barrier with its bytes.
     if (lane == 0) {
+      const bool is_a = warp == 0;
+      const uint32_t bytes = is_a ? (uint32_t)G::A_BYTES : (uint32_t)G::B_BYTES;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
         int tm, tn;
         tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+        const int m0 = tm * G::BM + (int)rank * G::HM;  // this CTA's rows of op(A)
+        const int n0 = tn * G::BN + (int)rank * G::HN;  // this CTA's columns of op(B)
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u) || *abort_flag) {
             if (!*abort_flag) watchdog_trip(watchdog, kSite2ProducerEmpty, abort_flag);
             ok = false;
             break;
           }
-          const int m0 = tm * G::BM + (int)rank * G::HM;  // this CTA's rows of op(A)
-          const int n0 = tn * G::BN + (int)rank * G::HN;  // this CTA's columns of op(B)
-          // Box coordinates (x = inner, y = outer) of the j-th box of each operand.
-          auto ax = [&](int j) { return AT ? m0 + j * G::BOX : kb * G::BK; };
-          auto ay = [&](int j) { return AT ? kb * G::BK : m0; };
-          auto bx = [&](int j) { return BT ? kb * G::BK : n0 + j * G::BOX; };
-          auto by = [&](int j) { return BT ? n0 : kb * G::BK; };
-          if constexpr (G::kSplit) {
-            // each CTA's split warps wait on its own full barrier
-            mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
+          // 3xTF32: each CTA's split warps wait on its own full barrier; else
+          // both CTAs' halves signal the even CTA's full barrier.
+          const uint32_t fb = G::kSplit ? full_bar(stage) : mapa_shared(full_bar(stage), 0);
+          if (G::kSplit)
+            mbar_arrive_expect_tx(full_bar(stage), bytes);
+          else if (leader)
+            mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
+          // An MN-major operand with a 3-D map comes in one instruction.
+          const bool one3d = is_a ? (AT && (mn3d & kA3d)) : (!BT && (mn3d & kB3d));
+          if (one3d) {
+            const uint32_t dst = is_a ? a_tile(stage) : b_tile(stage);
+            const CUtensorMap *map = is_a ? &tmap_a : &tmap_b;
+            const int z = (is_a ? m0 : n0) / G::BOX;
+            if constexpr (G::kSplit)
+              tma_load_3d(dst, map, fb, 0, kb * G::BK, z);
+            else
+              tma_load_3d_pair(dst, map, fb, 0, kb * G::BK, z);
+          } else if (is_a) {
 #pragma unroll
-            for (int j = 0; j < G::A_BOXES; ++j)
-              tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage), ax(j),
-                          ay(j));
-#pragma unroll
-            for (int j = 0; j < G::B_BOXES; ++j)
-              tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage), bx(j),
-                          by(j));
+            for (int j = 0; j < G::A_BOXES; ++j) {
+              const uint32_t dst = a_tile(stage) + j * G::A_BOX_BYTES;
+              const int x = AT ? m0 + j * G::BOX : kb * G::BK, y = AT ? kb * G::BK : m0;
+              if constexpr (G::kSplit)
+                tma_load_2d(dst, &tmap_a, fb, x, y);
+              else
+                tma_load_2d_pair(dst, &tmap_a, fb, x, y);
+            }
           } else {
-            // both halves signal the even CTA's full barrier
-            const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (uint32_t)G::RAW_BYTES);
 #pragma unroll
-            for (int j = 0; j < G::A_BOXES; ++j)
-              tma_load_2d_pair(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, fb, ax(j), ay(j));
-#pragma unroll
-            for (int j = 0; j < G::B_BOXES; ++j)
-              tma_load_2d_pair(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, fb, bx(j), by(j));
+            for (int j = 0; j < G::B_BOXES; ++j) {
+              const uint32_t dst = b_tile(stage) + j * G::B_BOX_BYTES;
+              const int x = BT ? kb * G::BK : n0 + j * G::BOX, y = BT ? n0 : kb * G::BK;
+              if constexpr (G::kSplit)
+                tma_load_2d(dst, &tmap_b, fb, x, y);
+              else
+                tma_load_2d_pair(dst, &tmap_b, fb, x, y);
+            }
           }
           if (++stage == G::STAGES) {
             stage = 0;
@@ -1022,18 +1054,47 @@ constexpr CUtensorMapDataType tma_type() {
 // as boxes of BK (one 128-byte swizzle row) x rows; MN-major operands as
 // boxes of 128 bytes of M or N x BK rows, with the 32-byte-atom swizzle for
 // 32-bit elements.
+// 3-D view of a row-major rows x cols matrix whose cols are a multiple of
+// `blk`: (c, r, j) -> X[r][j * blk + c], so that one box of blk x box_rows x
+// nblk lands in shared memory exactly as nblk 2-D boxes of blk x box_rows
+// side by side.  One TMA instruction then loads what took nblk.
+bool make_map3(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es, int64_t rows,
+               int64_t cols, int64_t ld, int blk, int box_rows, int nblk, CUtensorMapSwizzle swz) {
+  auto enc = get_encode();
+  if (!enc || cols % blk != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)blk, (cuuint64_t)rows, (cuuint64_t)(cols / blk)};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(blk * es)};
+  cuuint32_t box[3] = {(cuuint32_t)blk, (cuuint32_t)box_rows, (cuuint32_t)nblk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <class G, TcKind KIND>
 bool make_operand_maps(CUtensorMap *ta, CUtensorMap *tb, int M, int N, int K, const void *A,
-                       int64_t lda, const void *B, int64_t ldb, int rows_a, int cols_b) {
+                       int64_t lda, const void *B, int64_t ldb, int rows_a, int cols_b,
+                       int *mn3d) {
   const CUtensorMapDataType dt = tma_type<KIND>();
   const CUtensorMapSwizzle mn_swz =
       (G::k16 || G::k8) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
-  const bool ok_a = G::AT ? make_map(ta, A, dt, G::ES, K, M, lda, G::BOX, G::BK, mn_swz)
-                          : make_map(ta, A, dt, G::ES, M, K, lda, G::BK, rows_a,
-                                     CU_TENSOR_MAP_SWIZZLE_128B);
-  const bool ok_b = G::BT ? make_map(tb, B, dt, G::ES, N, K, ldb, G::BK, cols_b,
-                                     CU_TENSOR_MAP_SWIZZLE_128B)
-                          : make_map(tb, B, dt, G::ES, K, N, ldb, G::BOX, G::BK, mn_swz);
+  *mn3d = 0;
+  bool ok_a, ok_b;
+  if (G::AT && make_map3(ta, A, dt, G::ES, K, M, lda, G::BOX, G::BK, rows_a / G::BOX, mn_swz)) {
+    *mn3d |= kA3d;
+    ok_a = true;
+  } else {
+    ok_a = G::AT ? make_map(ta, A, dt, G::ES, K, M, lda, G::BOX, G::BK, mn_swz)
+                 : make_map(ta, A, dt, G::ES, M, K, lda, G::BK, rows_a, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!G::BT && make_map3(tb, B, dt, G::ES, K, N, ldb, G::BOX, G::BK, cols_b / G::BOX, mn_swz)) {
+    *mn3d |= kB3d;
+    ok_b = true;
+  } else {
+    ok_b = G::BT ? make_map(tb, B, dt, G::ES, N, K, ldb, G::BK, cols_b, CU_TENSOR_MAP_SWIZZLE_128B)
+                 : make_map(tb, B, dt, G::ES, K, N, ldb, G::BOX, G::BK, mn_swz);
+  }
   return ok_a && ok_b;
 }
 
@@ -1102,7 +1163,8 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
                        int *watchdog, cudaStream_t stream) {
   using G = Cfg<KIND, BN, AT, BT>;
   CUtensorMap ta, tb;
-  if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN))
+  int mn3d = 0;
+  if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN, &mn3d))
     return cudaErrorInvalidValue;
   auto kern = tc_gemm_kernel<KIND, BN, AT, BT>;
   static bool attr_set[64] = {};
@@ -1133,11 +1195,11 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m(32),
-                           watchdog, splits);
+                           watchdog, splits, mn3d);
   } else {
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                       raster_group_m(32), watchdog, 1);
+                                                       raster_group_m(32), watchdog, 1, mn3d);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) count_launch();
@@ -1150,7 +1212,8 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
                         cudaStream_t stream) {
   using G = Cfg2<KIND, AT, BT>;
   CUtensorMap ta, tb, tc;
-  if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, G::HM, G::HN))
+  int mn3d = 0;
+  if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, G::HM, G::HN, &mn3d))
     return cudaErrorInvalidValue;
   // C through TMA stores when its rows start on 16-byte boundaries.
   memset(&tc, 0, sizeof(tc));
@@ -1187,7 +1250,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   cfg.gridDim = dim3(2 * clusters);
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, C, M, N, K, ldc, c_tma ? 1 : 0,
-                         raster_group_m(16), watchdog);
+                         raster_group_m(16), watchdog, mn3d);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
