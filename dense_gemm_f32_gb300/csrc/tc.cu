@@ -295,7 +295,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         int tm, tn;
         tile_coords(unit_tile(u), tiles_m, tiles_n, group_m, tm, tn);
         for (int kb = unit_kb0(u); kb < unit_kb1(u); ++kb) {
-          if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+          if (!mbar_try_wait(empty_bar(stage), phase ^ 1u) &&
+              (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u))) {
             if (!*abort_flag) watchdog_trip(watchdog, kSiteProducerEmpty, abort_flag);
             ok = false;
             break;
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         const int kb0 = unit_kb0(u);
         for (int kb = kb0; kb < unit_kb1(u); ++kb) {
           const uint32_t ready = G::kSplit ? split_bar(stage) : full_bar(stage);
-          if (*abort_flag || !mbar_wait(ready, phase)) {
+          if (!mbar_try_wait(ready, phase) && (*abort_flag || !mbar_wait(ready, phase))) {
             if (!*abort_flag) watchdog_trip(watchdog, kSiteMmaFull, abort_flag);
             ok = false;
             break;
@@ -729,6 +730,9 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     if (lane == 0) {
       const bool is_a = warp == 0;
       const uint32_t bytes = is_a ? (uint32_t)G::A_BYTES : (uint32_t)G::B_BYTES;
+      // 3xTF32: each CTA's split warps wait on its own full barrier; else both
+      // CTAs' halves signal the even CTA's full barrier (stage s at +8 s).
+      const uint32_t fb0 = G::kSplit ? full_bar(0) : mapa_shared(full_bar(0), 0);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -738,14 +742,15 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
         const int m0 = tm * G::BM + (int)rank * G::HM;  // this CTA's rows of op(A)
         const int n0 = tn * G::BN + (int)rank * G::HN;  // this CTA's columns of op(B)
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u) || *abort_flag) {
+          // The abort flag is only consulted when the stage is not free yet:
+          // on the fast path nothing is waiting for this thread to stop.
+          if (!mbar_try_wait(empty_bar(stage), phase ^ 1u) &&
+              (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u))) {
             if (!*abort_flag) watchdog_trip(watchdog, kSite2ProducerEmpty, abort_flag);
             ok = false;
             break;
           }
-          // 3xTF32: each CTA's split warps wait on its own full barrier; else
-          // both CTAs' halves signal the even CTA's full barrier.
-          const uint32_t fb = G::kSplit ? full_bar(stage) : mapa_shared(full_bar(stage), 0);
+          const uint32_t fb = fb0 + 8u * (uint32_t)stage;
           if (G::kSplit)
             mbar_arrive_expect_tx(full_bar(stage), bytes);
           else if (leader)
@@ -819,7 +824,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * G::BN);
         for (int kb = 0; kb < kblocks; ++kb) {
           const uint32_t ready = G::kSplit ? ready_bar(stage) : full_bar(stage);
-          if (*abort_flag || !mbar_wait(ready, phase)) {
+          if (!mbar_try_wait(ready, phase) && (*abort_flag || !mbar_wait(ready, phase))) {
             if (!*abort_flag) watchdog_trip(watchdog, kSite2MmaFull, abort_flag);
             ok = false;
             break;
