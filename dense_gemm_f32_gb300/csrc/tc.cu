@@ -751,10 +751,10 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
             break;
           }
           const uint32_t fb = fb0 + 8u * (uint32_t)stage;
-          if (G::kSplit)
-            mbar_arrive_expect_tx(full_bar(stage), bytes);
-          else if (leader)
-            mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
+          // The copies are issued first and the expected bytes announced after
+          // them (the barrier's transaction count may run below zero in
+          // between; the phase still needs both producers' arrivals), which
+          // takes the arrival off the path from a free stage to its loads.
           // An MN-major operand with a 3-D map comes in one instruction.
           const bool one3d = is_a ? (AT && (mn3d & kA3d)) : (!BT && (mn3d & kB3d));
           if (one3d) {
@@ -786,6 +786,10 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
                 tma_load_2d_pair(dst, &tmap_b, fb, x, y);
             }
           }
+          if (G::kSplit)
+            mbar_arrive_expect_tx(full_bar(stage), bytes);
+          else if (leader)
+            mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1u;

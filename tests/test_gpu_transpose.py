@@ -81,3 +81,22 @@ def test_transposed_integer_bit_exact_large(mode, layout):
     C = _run(mode, A, B, ta, tb).cpu().numpy()
     exact = A.float().numpy().astype(np.int64) @ B.float().numpy().astype(np.int64)
     assert np.array_equal(C.astype(np.float64), exact.astype(np.float64))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
+@pytest.mark.parametrize("mode,pair", [mp for mp in _modes_and_kernels() if mp[0] != "simt"])
+def test_mn_major_operands_whole_blocks(mode, pair, layout, monkeypatch):
+    """M and N multiples of 128: an MN-major operand (A stored K x M, B
+    stored K x N) is read through a 3-D tensor map, one TMA load per stage
+    for all its 128-byte column blocks; K stays ragged."""
+    monkeypatch.setenv("DGEMM_TC_PAIR", pair)
+    ta, tb = layout
+    for (M, N, K) in [(256, 512, 200), (640, 384, 333), (128, 128, 1000)]:
+        A, B = inputs.make_random(M, N, K, seed=M + 2 * N + K, dist="normal",
+                                  dtype=gu.in_dtype(mode))
+        buf, C = gu.guarded_output(M, N, N + 4)
+        C = _run(mode, A, B, ta, tb, out=C)
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL[mode],
+                        f"{mode} pair={pair} {'T' if ta else 'N'}{'T' if tb else 'N'} {M}x{N}x{K}")
+        gu.assert_guards_intact(buf, M, N, N + 4)
