@@ -79,6 +79,7 @@ enum : int {
   kSiteMmaDrain = 0x23,
   kSiteEpiAccFull = 0x31,
   kSiteSplitFull = 0x41,
+  kSiteTestStall = 0x24,  // DGEMM_TC_TEST_STALL: the MMA thread's test wait ran out
 };
 
 // AT: A is stored K x M (op(A) = A^T), read MN-major.  BT: B is stored N x K
@@ -124,7 +125,7 @@ struct Cfg {
   static constexpr int kSplitWarp0 = 6, kSplitWarps = kSplit ? 4 : 0;
   static constexpr int THREADS = 32 * (2 + kEpiWarps + kSplitWarps);
   // barriers: full[S], empty[S], split[S], acc_full[2], acc_empty[2], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  static constexpr int NUM_BARS = 3 * STAGES + 6;  // + the test-stall barrier
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
   // K-split: the partial 128 x BN tile parked in the (then idle) stage area,
   // rows padded by 4 floats so that the epilogue's 16-byte row stores from 8
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
                    int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
-                   int splits, int mn3d) {
+                   int splits, int mn3d, int stall) {
   using G = Cfg<KIND, BN, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
   auto accf_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
+  const uint32_t stall_bar = bars + 8u * (3 * G::STAGES + 5);  // nothing ever arrives here
   uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::NUM_BARS * 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
       mbar_init(acce_bar(b), G::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -301,7 +304,6 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
           if (AT && (mn3d & kA3d)) {  // A stored K x M, all its column blocks at once
             tma_load_3d(a_tile(stage), &tmap_a, full_bar(stage), 0, kb * G::BK, tm * BM / G::BOX);
           } else {
@@ -326,6 +328,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
                             tn * BN + j * G::BOX_N, kb * G::BK);
             }
           }
+          // bytes announced after the copies are issued (see the pair kernel)
+          mbar_arrive_expect_tx(full_bar(stage), (uint32_t)G::RAW_BYTES);
           ++issued;
           if (++stage == G::STAGES) {
             stage = 0;
@@ -356,6 +360,12 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      if (stall && blockIdx.x == 0) {
+        // Test hook: wait on a barrier that nothing arrives at, so that the
+        // bounded wait runs out and the abort path below runs for real.
+        if (!mbar_wait(stall_bar, 0)) watchdog_trip(watchdog, kSiteTestStall, abort_flag);
+        ok = false;
+      }
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
           if (!*abort_flag) watchdog_trip(watchdog, kSiteMmaAccEmpty, abort_flag);
@@ -627,7 +637,7 @@ struct Cfg2 {
   static constexpr int kSplitWarp0 = kProdBWarp + 1, kSplitWarps = kSplit ? 8 : 0;
   static constexpr int THREADS = 32 * (3 + kEpiWarps + kSplitWarps);
   // full, empty, ready (3xTF32), accf[2], acce[2], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  static constexpr int NUM_BARS = 3 * STAGES + 6;  // + the test-stall barrier
   // epilogue staging: per epilogue warp two 32 x 32 fp32 chunks (TMA stores)
   static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;
   static constexpr int EPI_BYTES = kEpiWarps * 2 * EPI_CHUNK_BYTES;
@@ -653,6 +663,7 @@ enum : int {
   kSite2MmaTail = 0x64,
   kSite2EpiAccFull = 0x71,
   kSite2SplitFull = 0x81,
+  kSite2TestStall = 0x66,  // DGEMM_TC_TEST_STALL: the MMA thread's test wait ran out
 };
 
 template <TcKind KIND, bool AT, bool BT>
@@ -661,7 +672,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_c, float *__restrict__ C, int M,
                     int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog,
-                    int mn3d) {
+                    int mn3d, int stall) {
   using G = Cfg2<KIND, AT, BT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -676,6 +687,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
   auto accf_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
+  const uint32_t stall_bar = bars + 8u * (3 * G::STAGES + 5);  // nothing ever arrives here
   uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::EPI_BYTES + G::NUM_BARS * 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
@@ -704,6 +716,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
       mbar_init(acce_bar(b), 2 * G::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -818,6 +831,12 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      if (stall && cluster == 0) {
+        // Test hook: wait on a barrier that nothing arrives at, so that the
+        // bounded wait runs out and the abort path below runs for real.
+        if (!mbar_wait(stall_bar, 0)) watchdog_trip(watchdog, kSite2TestStall, abort_flag);
+        ok = false;
+      }
       for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
         if (*abort_flag || !mbar_wait(acce_bar(acc), acc_phase ^ 1u)) {
           if (!*abort_flag) watchdog_trip(watchdog, kSite2MmaAccEmpty, abort_flag);
@@ -1050,6 +1069,16 @@ int raster_group_m(int dflt) {
   return g ? g : dflt;
 }
 
+// DGEMM_TC_TEST_STALL=1 makes the MMA thread of the first CTA (pair) wait on
+// a barrier that nothing arrives at: its bounded wait runs out after ~2 s and
+// the kernel takes its abort path (watchdog site code, drained copies, freed
+// tensor memory, incomplete C).  For the failure-detection test only; read
+// at every launch.
+int test_stall() {
+  const char *e = getenv("DGEMM_TC_TEST_STALL");
+  return (e && e[0] == '1') ? 1 : 0;
+}
+
 template <TcKind KIND>
 constexpr CUtensorMapDataType tma_type() {
   return KIND == TcKind::kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -1204,11 +1233,12 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m(32),
-                           watchdog, splits, mn3d);
+                           watchdog, splits, mn3d, test_stall());
   } else {
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                       raster_group_m(32), watchdog, 1, mn3d);
+                                                       raster_group_m(32), watchdog, 1, mn3d,
+                                                       test_stall());
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) count_launch();
@@ -1259,7 +1289,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   cfg.gridDim = dim3(2 * clusters);
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, C, M, N, K, ldc, c_tma ? 1 : 0,
-                         raster_group_m(16), watchdog, mn3d);
+                         raster_group_m(16), watchdog, mn3d, test_stall());
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;

@@ -290,7 +290,10 @@ const char *dgemm_last_cuda_error(void);
  * up, drain its copies, free its tensor memory and return, leaving C
  * incomplete.  Returns DGEMM_OK when no kernel gave up since the last read,
  * DGEMM_ERR_WATCHDOG when one did (*where, if not NULL, gets the recorded
- * site code), DGEMM_ERR_CUDA on a CUDA error.
+ * site code), DGEMM_ERR_CUDA on a CUDA error.  With the environment variable
+ * DGEMM_TC_TEST_STALL=1 the first CTA of each tensor-core launch waits on a
+ * barrier that nothing arrives at, so that this path can be tested: the call
+ * returns after a few seconds with C incomplete and the status set.
  */
 int dgemm_watchdog_status(cudaStream_t stream, int *where);
 
