@@ -183,6 +183,15 @@ class ClockSampler:
         self.t0 = time.time()
         return self
 
+    def rows(self):
+        """Samples so far (the sampler keeps running)."""
+        if self.proc is None:
+            return []
+        time.sleep(0.12)  # let nvidia-smi write the samples of the window just ended
+        self.file.flush()
+        with open(self.file.name) as f:
+            return self._parse(f)
+
     def stop(self):
         rows = []
         if self.proc is None:
@@ -194,7 +203,15 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        for ln in self.file:
+        rows = self._parse(self.file)
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def _parse(lines):
+        rows = []
+        for ln in lines:
             c = [x.strip() for x in ln.split(",")]
             if len(c) < 9:
                 continue
@@ -206,9 +223,24 @@ class ClockSampler:
                                          "sw_thermal_slowdown": c[7], "sw_power_cap": c[8]}})
             except ValueError:
                 continue
-        self.file.close()
-        os.unlink(self.file.name)
         return rows
+
+
+# Throttle reasons that void a measurement (sw_power_cap is kept and noted).
+REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def rejected(clocks):
+    """Why a timed window's clock record voids it: a rejecting throttle
+    reason, or SM clocks far below their maximum with no reason (a leftover
+    clock lock).  None when the window is usable."""
+    bad = [r for r in clocks.get("reasons", []) if r in REJECT_REASONS]
+    if bad:
+        return ",".join(bad)
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    if sm and mx and sm < 0.8 * mx and not clocks.get("reasons"):
+        return f"sm clock {sm:.0f} of {mx:.0f} MHz with no reason"
+    return None
 
 
 def summarize_clocks(rows, windows):
@@ -557,6 +589,13 @@ def run_ours(args, dist):
     l2 = getattr(props, "L2_cache_size", 0) or (129 << 20)
     flush = l2_flush_buffer(device) if in_bytes < 2 * l2 else None
     r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device, ta, tb, flush=flush)
+    # A window whose clock record shows a rejecting throttle reason (or a
+    # clock lock) is measured once more; every rank takes the same decision.
+    why = rejected(summarize_clocks(sampler.rows(), [r["window"]]))
+    remeasured = None
+    if dist.max(1.0 if why else 0.0, device) > 0:
+        remeasured = why or "another rank's window"
+        r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device, ta, tb, flush=flush)
     del flush
     agg = aggregate(r["ms_total"], dist.world, w.flops, args.steps, lambda x: dist.max(x, device))
     windows = [r["window"]]
@@ -632,7 +671,8 @@ def run_ours(args, dist):
                                  f"{args.layout}",
                        "l2": ("inputs larger than L2 (no flush needed)" if r.get("flushed") is None
                               else "L2 flushed (2 x L2 bytes written) before every timed call"),
-                       "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+                       "parallelism": "replicas" if dist.world > 1 else "single GPU",
+                       "remeasured": remeasured},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e_line,

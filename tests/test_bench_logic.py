@@ -67,6 +67,19 @@ def test_clock_summary_inside_windows():
     assert bench.summarize_clocks([], [(0, 1)])["sm_mhz"] is None
 
 
+def test_rejected_clock_records():
+    """hw_slowdown / thermal reasons void a window (it is measured again);
+    sw_power_cap does not; clocks far below max with no reason do."""
+    assert bench.rejected({"reasons": ["sw_power_cap"], "sm_mhz": 1900.0, "sm_max_mhz": 2070.0}) is None
+    assert bench.rejected({"reasons": [], "sm_mhz": 2070.0, "sm_max_mhz": 2070.0}) is None
+    assert "hw_slowdown" in bench.rejected({"reasons": ["hw_slowdown"], "sm_mhz": 900.0,
+                                            "sm_max_mhz": 2070.0})
+    assert "sw_thermal_slowdown" in bench.rejected({"reasons": ["sw_power_cap", "sw_thermal_slowdown"],
+                                                    "sm_mhz": 1500.0, "sm_max_mhz": 2070.0})
+    assert "no reason" in bench.rejected({"reasons": [], "sm_mhz": 1200.0, "sm_max_mhz": 2070.0})
+    assert bench.rejected({"reasons": [], "sm_mhz": None, "sm_max_mhz": None}) is None
+
+
 def test_args_rules():
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
