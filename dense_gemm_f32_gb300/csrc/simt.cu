@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "launch.cuh"
 
 // This file is compiled once per operand layout: DGEMM_SIMT_UNIT = 2 * AT + BT
 // (AT: A stored K x M; BT: B stored N x K), so the layouts compile in
@@ -106,6 +107,8 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
                       int64_t ldc, int c_vec, int split_first, int split_parts,
                       float *__restrict__ work, unsigned int *__restrict__ counters) {
   constexpr int BM = G::BM, BN = G::BN, BK = G::BK, TM = G::TM, TN = G::TN;
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel on the stream has completed
   // A stored k-major (transposed): a 128-bit load gives 4 consecutive rows.
   extern __shared__ float4 simt_smem[];
   auto As = reinterpret_cast<float(*)[BK][G::AROW]>(simt_smem);
@@ -401,9 +404,9 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
     e = cudaMemsetAsync(counters, 0, (size_t)rem * sizeof(unsigned int), stream);
   }
   if (e == cudaSuccess) {
-    kern<<<(unsigned)grid, G::THREADS, G::SMEM_BYTES, stream>>>(
-        M, N, K, A, lda, B, ldb, C, ldc, c_vec, (int)split_first, parts, work, counters);
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream, 1, M, N,
+                      K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0, (int)split_first, parts, work,
+                      counters);
   }
   if (scratch) {
     const cudaError_t e2 = scratch_free(scratch, stream);
@@ -414,6 +417,8 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
 
 #if DGEMM_SIMT_UNIT == 0
 __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ldc) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t total = (int64_t)M * N;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -469,8 +474,8 @@ cudaError_t launch_zero_fill(float *C, int M, int N, int64_t ldc, int num_sms,
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  zero_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(C, M, N, ldc);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      launch_kernel(zero_fill_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 1, C, M, N, ldc);
   if (e == cudaSuccess) count_launch();
   return e;
 }

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace dg {
 namespace {
@@ -24,6 +25,8 @@ __global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_byte
   // the unaligned source row, one 128-bit store; columns past the row are
   // zeroed.  Rows run along y, chunks along x, so there is no division per
   // element.
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t chunks = ldd_bytes / 16;
   for (int r = blockIdx.y; r < rows; r += gridDim.y) {
     const uint8_t *srow = src + (int64_t)r * lds_bytes;
@@ -72,6 +75,8 @@ __global__ void __launch_bounds__(256)
     transpose8_kernel(const uint8_t *__restrict__ src, int64_t lds, uint8_t *__restrict__ dst,
                       int64_t ldd, int rows, int cols, int words_ok) {
   __shared__ uint32_t tile[kT][kT / 4 + 1];
+  pdl_launch_dependents();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int tiles_c = (cols + kT - 1) / kT;
   const int64_t ntiles = (int64_t)((rows + kT - 1) / kT) * tiles_c;
@@ -116,10 +121,10 @@ cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t l
   if (grid > ntiles) grid = ntiles;
   const bool words_ok = reinterpret_cast<uintptr_t>(src) % 4 == 0 && lds % 4 == 0 &&
                         reinterpret_cast<uintptr_t>(dst) % 4 == 0 && ldd % 4 == 0;
-  transpose8_kernel<<<(unsigned)grid, 256, 0, stream>>>(
-      static_cast<const uint8_t *>(src), lds, static_cast<uint8_t *>(dst), ldd, rows, cols,
-      words_ok ? 1 : 0);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_kernel(transpose8_kernel, dim3((unsigned)grid), dim3(256), 0, stream, 1,
+                                      static_cast<const uint8_t *>(src), lds,
+                                      static_cast<uint8_t *>(dst), ldd, rows, cols,
+                                      words_ok ? 1 : 0);
   if (e == cudaSuccess) count_launch();
   return e;
 }
@@ -133,10 +138,11 @@ cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd,
   if (by > rows) by = rows;
   if (by > 65535) by = 65535;
   if (by < 1) by = 1;
-  repitch_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(
-      static_cast<const uint8_t *>(src), lds * elem_bytes, static_cast<uint8_t *>(dst),
-      ldd * elem_bytes, rows, (int64_t)cols * elem_bytes, elem_bytes);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_kernel(repitch_kernel, dim3((unsigned)bx, (unsigned)by), dim3(256), 0,
+                                      stream, 1, static_cast<const uint8_t *>(src),
+                                      lds * elem_bytes, static_cast<uint8_t *>(dst),
+                                      ldd * elem_bytes, rows, (int64_t)cols * elem_bytes,
+                                      elem_bytes);
   if (e == cudaSuccess) count_launch();
   return e;
 }

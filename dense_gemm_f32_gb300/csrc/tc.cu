@@ -38,6 +38,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 // This file is compiled once per operand layout: DGEMM_TC_UNIT = 2 * AT + BT
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
                    int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
                    int splits, int mn3d, int stall) {
   using G = Cfg<KIND, BN, AT, BT>;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // set-up done; the previous kernel on the stream has completed
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -674,6 +677,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
                     int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog,
                     int mn3d, int stall) {
   using G = Cfg2<KIND, AT, BT>;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -735,6 +739,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
   cluster_sync();  // the peer's barriers are initialised before any signal crosses
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // set-up done; the previous kernel on the stream has completed
 
   if (warp == 0 || warp == G::kProdBWarp) {
     // ----------------------------------------------------------- producers
@@ -1218,29 +1223,12 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int kblocks = (K + G::BK - 1) / G::BK;
   const int splits = choose_splits(kern, G::THREADS, G::SMEM_BYTES, dev, tiles, kblocks, num_sms);
-  if (splits > 1) {
-    // one unit per CTA, the `splits` parts of a tile in one cluster
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(tiles * splits), 1, 1);
-    cfg.blockDim = dim3(G::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = G::SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0, raster_group_m(32),
-                           watchdog, splits, mn3d, test_stall());
-  } else {
-    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    kern<<<grid, G::THREADS, G::SMEM_BYTES, stream>>>(ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
-                                                       raster_group_m(32), watchdog, 1, mn3d,
-                                                       test_stall());
-    e = cudaGetLastError();
-  }
+  // K-split: one unit per CTA, the `splits` parts of a tile in one cluster;
+  // else a persistent grid of at most one CTA per SM.
+  const int64_t grid = splits > 1 ? tiles * splits : (tiles < num_sms ? tiles : num_sms);
+  e = launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream,
+                    splits > 1 ? (unsigned)splits : 1u, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
+                    raster_group_m(32), watchdog, splits, mn3d, test_stall());
   if (e == cudaSuccess) count_launch();
   return e;
 }
@@ -1287,9 +1275,9 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
-  cfg.gridDim = dim3(2 * clusters);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, C, M, N, K, ldc, c_tma ? 1 : 0,
-                         raster_group_m(16), watchdog, mn3d, test_stall());
+  e = launch_kernel(kern, dim3(2 * clusters), dim3(G::THREADS), G::SMEM_BYTES, stream, 2u, ta, tb,
+                    tc, C, M, N, K, ldc, c_tma ? 1 : 0, raster_group_m(16), watchdog, mn3d,
+                    test_stall());
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
@@ -1319,6 +1307,7 @@ cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const v
 
 #if DGEMM_TC_UNIT == 0
 __global__ void read_watchdog_kernel(int *out) {
+  pdl_wait();
   *out = g_watchdog;
   g_watchdog = 0;
 }
@@ -1396,8 +1385,7 @@ cudaError_t read_watchdog(cudaStream_t stream, int *code) {
   int *d = nullptr;
   cudaError_t e = scratch_alloc(reinterpret_cast<void **>(&d), sizeof(int), stream);
   if (e != cudaSuccess) return e;
-  read_watchdog_kernel<<<1, 1, 0, stream>>>(d);
-  e = cudaGetLastError();
+  e = launch_kernel(read_watchdog_kernel, dim3(1), dim3(1), 0, stream, 1, d);
   if (e == cudaSuccess) count_launch();
   int h = 0;
   if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(int), cudaMemcpyDeviceToHost, stream);
