@@ -8,17 +8,23 @@
 // multi-buffered copy pipeline (sections 二十三-二十五).
 //
 // Blackwell design (none of this is on the pages, which stop at WMMA):
-//  * Persistent kernel, one CTA per SM, walking 128 x BN output tiles in
+//  * Two persistent kernels: tc_gemm_kernel, one CTA per SM walking 128 x BN
+//    output tiles, and tc2_gemm_kernel, CTA pairs (clusters of 2) walking
+//    256 x 256 tiles with tcgen05.mma.cta_group::2; tiles are visited in
 //    groups of tile rows (L2 reuse of the A and B panels; see raster_group_m).
-//  * Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma (one
-//    thread) and owns the TMEM allocation, warps 2-5 drain the accumulator
-//    (tcgen05.ld -> registers -> global).  For 3xTF32, warps 6-9 split each
-//    staged fp32 tile into hi and lo TF32 parts in shared memory.
+//  * Warp roles: TMA producer(s) (the pair kernel has one thread per
+//    operand, warps 0 and 6), warp 1 issues tcgen05.mma (one thread) and owns
+//    the TMEM allocation, warps 2-5 drain the accumulator (tcgen05.ld ->
+//    registers -> global, or shared memory and TMA stores).  For 3xTF32 the
+//    remaining warps split each staged fp32 tile into hi and lo TF32 parts.
 //  * Operands: A (M x K, K contiguous) is K-major, B (K x N, N contiguous) is
-//    MN-major; both arrive by 2-D TMA boxes of one 128-byte swizzle row width
-//    into 128B-swizzled shared memory, which is the layout the MMA's shared
-//    memory descriptors describe.  TMA fills the out-of-range part of an edge
-//    box with zeros (the pages' zero-fill of partial tiles, section 二十六).
+//    MN-major (either may be stored transposed instead); they arrive by TMA
+//    boxes of one 128-byte swizzle row width into 128B-swizzled shared
+//    memory, the layout the MMA's shared-memory descriptors describe; an
+//    MN-major operand whose extent allows it comes through a 3-D tensor map,
+//    one instruction for all its column blocks.  TMA fills the out-of-range
+//    part of an edge box with zeros (the pages' zero-fill of partial tiles,
+//    section 二十六).
 //  * Accumulators: fp32 in tensor memory, two buffers of BN columns each, so
 //    the epilogue of tile i overlaps the main loop of tile i + 1.
 //  * Problems with too few tiles to occupy the GPU split each tile along K

@@ -174,7 +174,8 @@ int gemm_bf16_tc(int M, int N, int K,
  *
  * Same arguments, semantics, accuracy and status codes as gemm_f32_tc.  The
  * difference is where the re-pitch scratch lives: gemm_f32_tc takes it from
- * cudaMallocAsync when A or B rows do not start on 16-byte boundaries; this
+ * the library's stream-ordered memory pool when A or B rows do not start on
+ * 16-byte boundaries; this
  * entry point uses instead a fixed 16 MiB array (DGEMM_NOALLOC_SCRATCH_BYTES)
  * that the library holds in device memory on every GPU that loads it, until
  * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
