@@ -213,12 +213,14 @@ __device__ __forceinline__ void watchdog_trip(int *watchdog, int site, volatile 
 // test), so the raw fp32 tile itself serves as hi = trunc_tf32(x) and only lo
 // is written: lo = x - hi, exact in fp32, rounded to TF32 (nearest, ties
 // away).  The dropped lo*lo term and the rounding of lo are each below
-// 2^-20 |x y| per product.
+// 2^-20 |x y| per product.  Infinities and NaNs have no low part (x - x
+// would be NaN and turn an infinite result into NaN): their lo is 0 and the
+// raw value carries them, as in the plain TF32 product.
 __device__ __forceinline__ uint32_t split_lo_tf32(uint32_t xbits) {
   const float r = __uint_as_float(xbits) - __uint_as_float(xbits & 0xFFFFE000u);
   uint32_t l;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
-  return l;
+  return (xbits & 0x7F800000u) == 0x7F800000u ? 0u : l;
 }
 
 template <TcKind KIND, int BN, bool AT, bool BT>

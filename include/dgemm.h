@@ -135,7 +135,10 @@ int gemm_f32_simt(int M, int N, int K,
  * mode = DGEMM_TC_3XTF32: each operand is split a ~ hi + lo (hi = a with the
  *                         low 13 mantissa bits cleared, lo = a - hi rounded
  *                         to TF32) and C = A_hi B_hi + A_hi B_lo + A_lo B_hi;
- *                         accuracy <= 1e-5 * (|A| x |B|).
+ *                         accuracy <= 1e-5 * (|A| x |B|).  Infinities and
+ *                         NaNs propagate as in IEEE arithmetic, except that
+ *                         an infinite entry meeting a finite one whose lo is
+ *                         exactly 0 adds inf * 0 = NaN to that entry of C.
  * Argument layout as gemm_f32_simt.  Unknown mode: DGEMM_ERR_UNSUPPORTED.
  */
 int gemm_f32_tc(int mode, int M, int N, int K,
