@@ -62,7 +62,12 @@ def parse_args(argv=None):
     p.add_argument("--shape", default=None,
                    help="M,N,K: time the headline mode on a seeded uniform[-1,1) workload of this "
                         "shape instead of the benchmark workload (profiling runs)")
+    p.add_argument("--quick", action="store_true",
+                   help="smoke run: every workload of the configuration once (1 timed step, 3 "
+                        "warm-up, no CPU baseline, no end-to-end leg, 2 steps per mode)")
     a = p.parse_args(argv)
+    if a.quick:
+        a.steps, a.warmup, a.no_cpu, a.no_e2e = 1, 3, True, True
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
     if a.steps < 1:
@@ -629,21 +634,23 @@ def run_ours(args, dist):
         for m, tr in table:
             wm = workload_for(m, transformer=tr)
             if m == mode and wm.name == w.name:
-                res = {"ms_per_step": statistics.median(r["per_step_ms"])}
+                per = r["per_step_ms"]
             else:
                 _, _, Adm, Bdm = device_inputs(wm, m, device)
                 Cm = torch.empty((wm.M, wm.N), dtype=torch.float32, device=device)
-                steps_m = max(5, min(args.steps, 20))
+                steps_m = 2 if args.quick else max(5, min(args.steps, 20))
                 rm = time_device(m, Adm, Bdm, Cm, steps_m, 3, dist, device)
                 windows.append(rm["window"])
-                res = {"ms_per_step": statistics.median(rm["per_step_ms"])}
+                per = rm["per_step_ms"]
                 del Adm, Bdm, Cm
                 torch.cuda.empty_cache()
             bm, pm, _ = mode_peak(m, peaks, num_sms)
-            tfl = wm.flops / (res["ms_per_step"] * 1e-3) / 1e12
+            med = statistics.median(per)
+            tfl = wm.flops / (med * 1e-3) / 1e12
             modes[f"{m}@{wm.name}"] = {"tflops_median": round(tfl, 2), "bound": bm,
                                        "peak": round(pm, 1), "frac": round(tfl / pm, 4),
-                                       "ms_median": round(res["ms_per_step"], 4)}
+                                       "ms_median": round(med, 4), "ms_min": round(min(per), 4),
+                                       "ms_max": round(max(per), 4), "steps": len(per)}
     small = {}
     if not args.no_modes and not args.shape:
         small, sw = time_small(device, dist)

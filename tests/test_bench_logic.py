@@ -85,6 +85,8 @@ def test_args_rules():
         bench.parse_args(["--warmup", "2"])
     a = bench.parse_args([])
     assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1 and a.impl == "ours"
+    q = bench.parse_args(["--quick"])  # every workload once, still >= 3 warm-up steps
+    assert q.steps == 1 and q.warmup == 3 and q.no_cpu and q.no_e2e and not q.no_modes
 
 
 def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
