@@ -443,6 +443,44 @@ def time_device(mode, Ad, Bd, C, steps, warmup, dist, device, ta=False, tb=False
             "flushed": None if flush is None else True}
 
 
+def cublas_same_run(mode, Ad, Bd, device, steps=10):
+    """cuBLAS (through torch) on the headline's operands, timed the same way:
+    a comparator for the roofline fraction, not part of the library.  None
+    for modes cuBLAS has no counterpart of (3xTF32) or when the call fails."""
+    import torch
+
+    try:
+        if mode in ("tf32", "simt"):
+            prev = torch.backends.cuda.matmul.allow_tf32
+            torch.backends.cuda.matmul.allow_tf32 = mode == "tf32"
+            fn = lambda: Ad @ Bd  # noqa: E731
+            restore = lambda: setattr(torch.backends.cuda.matmul, "allow_tf32", prev)  # noqa: E731
+        elif mode in ("bf16", "fp16"):
+            fn = lambda: torch.mm(Ad, Bd, out_dtype=torch.float32)  # noqa: E731
+            restore = lambda: None  # noqa: E731
+        elif mode in ("e4m3", "e5m2"):
+            Bt = Bd.t().contiguous().t()  # column-major B, as cuBLAS's FP8 kernels want
+            one = torch.tensor(1.0, device=device)
+            fn = lambda: torch._scaled_mm(Ad, Bt, scale_a=one, scale_b=one,  # noqa: E731
+                                          out_dtype=torch.float32)
+            restore = lambda: None  # noqa: E731
+        else:
+            return None
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        for i in range(steps):
+            ev[i].record()
+            fn()
+        ev[steps].record()
+        torch.cuda.synchronize(device)
+        restore()
+        return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    except Exception:  # noqa: BLE001 -- a comparator must never fail the bench
+        return None
+
+
 def time_graph(mode, Ad, Bd, C, device, calls=20, replays=5):
     """Device time per call of `calls` back-to-back calls captured in one CUDA
     graph (no host launch gaps; L2 warm after the first call)."""
@@ -614,6 +652,14 @@ def run_ours(args, dist):
                 "peak_source": f"{peak_src}: {peak_how}",
                 "per_launch_flops": w.flops, "launches_per_step": launches_per_step}
 
+    # ---- cuBLAS on the same operands (comparator for the roofline fraction)
+    if not args.quick and not ta and not tb and dist.world == 1:
+        ms_cublas = cublas_same_run(mode, Ad, Bd, device)
+        if ms_cublas:
+            tf = w.flops / (ms_cublas * 1e-3) / 1e12
+            roofline["cublas_same_run"] = {"tflops": round(tf, 1),
+                                           "frac_of_cublas": round(achieved / tf, 4)}
+
     # ---- end to end through the public API with host buffers
     e2e_line = None
     del Ad, Bd, C
@@ -651,6 +697,8 @@ def run_ours(args, dist):
                                        "peak": round(pm, 1), "frac": round(tfl / pm, 4),
                                        "ms_median": round(med, 4), "ms_min": round(min(per), 4),
                                        "ms_max": round(max(per), 4), "steps": len(per)}
+            if m == "3xtf32":  # three TF32 products per product: the tensor pipe's share
+                modes[f"{m}@{wm.name}"]["mma_frac"] = round(3 * tfl / pm, 4)
     small = {}
     if not args.no_modes and not args.shape:
         small, sw = time_small(device, dist)
