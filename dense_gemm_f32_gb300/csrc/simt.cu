@@ -23,6 +23,7 @@
 //    (template kVec); ragged edges fall back to masked scalar loads.
 //  * Thread blocks walk the C tiles in groups of 8 tile rows so that panels
 //    of A and B are re-read from L2 instead of HBM.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -370,14 +371,14 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   auto kern = ab_vec ? sgemm_simt_kernel<G, true, AT, BT> : sgemm_simt_kernel<G, false, AT, BT>;
   if (G::SMEM_BYTES > 48 * 1024) {
     // opt in to more than 48 KB of dynamic shared memory (per device, once)
-    static bool done[2][64] = {};
+    static std::atomic<bool> done[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !done[ab_vec][dev]) {
+    if (dev < 0 || dev >= 64 || !done[ab_vec][dev].load(std::memory_order_acquire)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) done[ab_vec][dev] = true;
+      if (dev >= 0 && dev < 64) done[ab_vec][dev].store(true, std::memory_order_release);
     }
   }
   // Tail split: when the tiles leave a last wave that is at most half full,

@@ -1218,14 +1218,14 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN, &mn3d))
     return cudaErrorInvalidValue;
   auto kern = tc_gemm_kernel<KIND, BN, AT, BT>;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
@@ -1255,7 +1255,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   const bool c_tma = c_vec && make_map(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32,
                                        32, CU_TENSOR_MAP_SWIZZLE_128B);
   auto kern = tc2_gemm_kernel<KIND, AT, BT>;
-  static int max_clusters[64] = {};
+  static std::atomic<int> max_clusters[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1270,7 +1270,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int maxc = (dev >= 0 && dev < 64) ? max_clusters[dev] : 0;
+  int maxc = (dev >= 0 && dev < 64) ? max_clusters[dev].load(std::memory_order_acquire) : 0;
   if (maxc == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -1278,7 +1278,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
     e = cudaOccupancyMaxActiveClusters(&maxc, (void *)kern, &cfg);
     if (e != cudaSuccess) return e;
     if (maxc < 1) return cudaErrorInvalidConfiguration;
-    if (dev >= 0 && dev < 64) max_clusters[dev] = maxc;
+    if (dev >= 0 && dev < 64) max_clusters[dev].store(maxc, std::memory_order_release);
   }
   const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
@@ -1359,15 +1359,17 @@ cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, in
 namespace {
 // Device address of this device's watchdog word (looked up once per device).
 int *watchdog_address() {
-  static int *addr[64] = {};
+  static std::atomic<int *> addr[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (addr[dev] == nullptr) {
+  int *a = addr[dev].load(std::memory_order_acquire);
+  if (a == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_watchdog) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<int *>(p);
+    a = static_cast<int *>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
 }
 }  // namespace
 

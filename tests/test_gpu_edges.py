@@ -174,3 +174,41 @@ def test_simt_tail_split_around_wave_boundaries():
         assert torch.equal(C1, C2), "split sums must not depend on which part finishes last"
         ref, S = gu.oracle_full(A, B)
         gu.assert_close(C2.cpu().numpy(), ref, S, gu.TOL["simt"], f"simt tail {M}x{N}x{K}")
+
+
+def test_concurrent_calls_from_host_threads():
+    """Four host threads, each on its own stream, call different paths at
+    once (re-pitch scratch from the shared pool, cluster K-split, FP8
+    transpose, SIMT tail split): every result must match the oracle."""
+    import threading
+
+    cases = [("tf32", (1000, 1013, 997)), ("bf16", (1024, 1024, 1024)),
+             ("e4m3", (520, 700, 640)), ("simt", (640, 512, 777))]
+    data = []
+    for mode, (M, N, K) in cases:
+        A, B = inputs.make_random(M, N, K, seed=M + K, dist="normal", dtype=gu.in_dtype(mode))
+        data.append((mode, A, B, A.cuda(), B.cuda()))
+    torch.cuda.synchronize()
+    results, errors = [None] * len(data), []
+
+    def work(i):
+        try:
+            mode, _, _, Ad, Bd = data[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    C = dg.matmul(Ad, Bd, mode=mode, stream=s)
+            s.synchronize()
+            results[i] = C.cpu()
+        except Exception as e:  # noqa: BLE001 -- reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(data))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for (mode, A, B, _, _), C in zip(data, results):
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(C.numpy(), ref, S, gu.TOL[mode], f"{mode} from a host thread")
