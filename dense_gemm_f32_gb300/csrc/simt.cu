@@ -29,6 +29,7 @@
 
 #include "kernels.h"
 #include "launch.cuh"
+#include "ptx.cuh"
 
 // This file is compiled once per operand layout: DGEMM_SIMT_UNIT = 2 * AT + BT
 // (AT: A stored K x M; BT: B stored N x K), so the layouts compile in
@@ -95,6 +96,11 @@ struct SimtCfg {
   static_assert(A_VECS >= 1 && B_VECS >= 1, "every thread loads A and B");
   static_assert(BM * BK % (4 * THREADS) == 0 && BK * BN % (4 * THREADS) == 0, "even loads");
   static constexpr int SMEM_BYTES = 2 * BK * AROW * 4 + 2 * BK * BROW * 4;  // two buffers
+  // Cluster K-split: a part's BM x BN partial tile parked in shared memory,
+  // rows padded by 4 floats.
+  static constexpr int PART_PITCH = BN + 4;
+  static constexpr int PART_BYTES = BM * PART_PITCH * 4;
+  static constexpr int SMEM_CLUSTER = SMEM_BYTES > PART_BYTES ? SMEM_BYTES : PART_BYTES;
 };
 
 // AT: A is stored K x M (op(A) = A^T); BT: B is stored N x K (op(B) = B^T).
@@ -106,7 +112,8 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     sgemm_simt_kernel(int M, int N, int K, const float *__restrict__ A, int64_t lda,
                       const float *__restrict__ B, int64_t ldb, float *__restrict__ C,
                       int64_t ldc, int c_vec, int split_first, int split_parts,
-                      float *__restrict__ work, unsigned int *__restrict__ counters) {
+                      float *__restrict__ work, unsigned int *__restrict__ counters,
+                      int cluster_parts) {
   constexpr int BM = G::BM, BN = G::BN, BK = G::BK, TM = G::TM, TN = G::TN;
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel on the stream has completed
@@ -273,6 +280,60 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
       asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[i][2 * h]), "=f"(acc[i][2 * h + 1]) : "l"(acc2[i][h]));
 #endif
 
+  if (split && cluster_parts) {
+    // Every tile is split and the parts of a tile form one thread-block
+    // cluster (CTA rank = part): park the partial tile in this CTA's shared
+    // memory (free since the main loop's last barrier), then each CTA adds
+    // one slice of the tile's rows over all parts, in part order, through
+    // distributed shared memory and writes it to C.  Every thread reaches
+    // both cluster barriers.
+    float *park = reinterpret_cast<float *>(simt_smem);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int rl = row_base + (i / 4) * G::LM * 4 + (i % 4);
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h)
+        *reinterpret_cast<float4 *>(park + rl * G::PART_PITCH + col_base + h * G::LN * 4) =
+            make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
+    }
+    __syncwarp();
+    cluster_sync();  // partials written (release) and visible (acquire)
+    const int rank = (int)cluster_ctarank();
+    const int r0 = (BM * rank) / split_parts, r1 = (BM * (rank + 1)) / split_parts;
+    constexpr int Q = BN / 4;
+    const uint32_t base = smem_u32(park);
+    uint32_t peer[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) peer[p] = p < split_parts ? mapa_shared(base, (uint32_t)p) : 0u;
+    for (int e = tid; e < (r1 - r0) * Q; e += G::THREADS) {
+      const int rl = r0 + e / Q, cl = 4 * (e % Q);
+      const uint32_t off = (uint32_t)((rl * G::PART_PITCH + cl) * 4);
+      float4 v[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+        if (p < split_parts) v[p] = ld_cluster_f4(peer[p] + off);
+      float4 sum = v[0];  // parts added in K order
+#pragma unroll
+      for (int p = 1; p < 8; ++p)
+        if (p < split_parts) sum.x += v[p].x, sum.y += v[p].y, sum.z += v[p].z, sum.w += v[p].w;
+      const int r = m0 + rl, c = n0 + cl;
+      if (r < M) {
+        float *d = C + (int64_t)r * ldc + c;
+        if (c_vec && c + 3 < N) {
+          *reinterpret_cast<float4 *>(d) = sum;
+        } else {
+          if (c < N) d[0] = sum.x;
+          if (c + 1 < N) d[1] = sum.y;
+          if (c + 2 < N) d[2] = sum.z;
+          if (c + 3 < N) d[3] = sum.w;
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while a peer may still read its partial
+    return;
+  }
+
   if (split) {
     // Park this part's partial tile; the last part to finish sums all parts
     // in part order (so the result does not depend on which finishes last)
@@ -369,14 +430,15 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   auto kern = ab_vec ? sgemm_simt_kernel<G, true, AT, BT> : sgemm_simt_kernel<G, false, AT, BT>;
-  if (G::SMEM_BYTES > 48 * 1024) {
-    // opt in to more than 48 KB of dynamic shared memory (per device, once)
+  {
+    // opt in to the dynamic shared memory of the cluster K-split (per device, once)
     static std::atomic<bool> done[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !done[ab_vec][dev].load(std::memory_order_acquire)) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_BYTES);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               G::SMEM_CLUSTER);
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) done[ab_vec][dev].store(true, std::memory_order_release);
     }
@@ -394,6 +456,14 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   unsigned int *counters = nullptr;
   void *scratch = nullptr;
   cudaError_t e = cudaSuccess;
+  if (parts > 1 && rem == tiles) {
+    // Every tile is split (a small problem): the parts of a tile run as one
+    // cluster and add their partials through distributed shared memory; no
+    // scratch, no second pass.
+    return launch_kernel(kern, dim3((unsigned)(tiles * parts)), dim3(G::THREADS), G::SMEM_CLUSTER,
+                         stream, (unsigned)parts, M, N, K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0,
+                         0, parts, nullptr, nullptr, 1);
+  }
   if (parts > 1) {
     split_first = tiles - rem;
     grid = split_first + rem * parts;
@@ -407,7 +477,7 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   if (e == cudaSuccess) {
     e = launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream, 1, M, N,
                       K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0, (int)split_first, parts, work,
-                      counters);
+                      counters, 0);
   }
   if (scratch) {
     const cudaError_t e2 = scratch_free(scratch, stream);

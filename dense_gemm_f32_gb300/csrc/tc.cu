@@ -223,6 +223,18 @@ __device__ __forceinline__ uint32_t split_lo_tf32(uint32_t xbits) {
   return (xbits & 0x7F800000u) == 0x7F800000u ? 0u : l;
 }
 
+// The split's fast path: the same lo without the infinity / NaN test, and
+// `seen` becomes NaN if any x was infinite or NaN (x - x is NaN then), one
+// max.NaN per element; the caller redoes its elements with split_lo_tf32
+// in that (rare) case.
+__device__ __forceinline__ uint32_t split_lo_tf32_fast(uint32_t xbits, float &seen) {
+  const float r = __uint_as_float(xbits) - __uint_as_float(xbits & 0xFFFFE000u);
+  asm("max.NaN.f32 %0, %0, %1;" : "+f"(seen) : "f"(r));
+  uint32_t l;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
+  return l;
+}
+
 template <TcKind KIND, int BN, bool AT, bool BT>
 __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -515,10 +527,18 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
         // lo copy.
         uint4 *raw = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES);
         uint4 *lo = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES + G::RAW_BYTES);
+        float seen = 0.f;
         for (int i = t; i < G::RAW_BYTES / 16; i += 32 * G::kSplitWarps) {
           const uint4 v = raw[i];
-          lo[i] = make_uint4(split_lo_tf32(v.x), split_lo_tf32(v.y), split_lo_tf32(v.z),
-                             split_lo_tf32(v.w));
+          lo[i] = make_uint4(split_lo_tf32_fast(v.x, seen), split_lo_tf32_fast(v.y, seen),
+                             split_lo_tf32_fast(v.z, seen), split_lo_tf32_fast(v.w, seen));
+        }
+        if (seen != seen) {  // an infinity or NaN in this thread's elements
+          for (int i = t; i < G::RAW_BYTES / 16; i += 32 * G::kSplitWarps) {
+            const uint4 v = raw[i];
+            lo[i] = make_uint4(split_lo_tf32(v.x), split_lo_tf32(v.y), split_lo_tf32(v.z),
+                               split_lo_tf32(v.w));
+          }
         }
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         __syncwarp();
@@ -1006,6 +1026,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
         constexpr int kStride = 32 * G::kSplitWarps;
         constexpr int kIters = G::RAW_BYTES / 16 / kStride;
         static_assert(kIters % 4 == 0, "the split loop is unrolled by 4");
+        float seen = 0.f;
 #pragma unroll 1
         for (int it = 0; it < kIters; it += 4) {
           uint4 v[4];
@@ -1014,8 +1035,15 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             lo[t + (it + u) * kStride] =
-                make_uint4(split_lo_tf32(v[u].x), split_lo_tf32(v[u].y), split_lo_tf32(v[u].z),
-                           split_lo_tf32(v[u].w));
+                make_uint4(split_lo_tf32_fast(v[u].x, seen), split_lo_tf32_fast(v[u].y, seen),
+                           split_lo_tf32_fast(v[u].z, seen), split_lo_tf32_fast(v[u].w, seen));
+        }
+        if (seen != seen) {  // an infinity or NaN in this thread's elements
+          for (int i = t; i < G::RAW_BYTES / 16; i += kStride) {
+            const uint4 v = raw[i];
+            lo[i] = make_uint4(split_lo_tf32(v.x), split_lo_tf32(v.y), split_lo_tf32(v.z),
+                               split_lo_tf32(v.w));
+          }
         }
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         __syncwarp();
