@@ -212,3 +212,29 @@ def test_concurrent_calls_from_host_threads():
     for (mode, A, B, _, _), C in zip(data, results):
         ref, S = gu.oracle_full(A, B)
         gu.assert_close(C.numpy(), ref, S, gu.TOL[mode], f"{mode} from a host thread")
+
+
+def test_dependent_calls_back_to_back():
+    """Calls queued without synchronisation where each reads what the one
+    before wrote (read after write) or overwrites what the one before read
+    (write after read), across paths and kernels.  Every kernel starts early
+    under programmatic dependent launch and must wait for its predecessor
+    before touching memory."""
+    M = 640
+    g = torch.Generator().manual_seed(71)
+    X0 = torch.randn(M, M, generator=g) / 8
+    W = [torch.randn(M, M, generator=g) / 8 for _ in range(3)]
+    Xd, Wd = X0.cuda(), [w.cuda() for w in W]
+    Y1 = dg.matmul(Xd, Wd[0], mode="3xtf32")                 # Y1 = X0 W0
+    Y2 = dg.matmul(Y1, Wd[1], mode="simt")                   # reads Y1 (RAW)
+    dg.matmul(Y2, Wd[2], mode="3xtf32", out=Xd)              # overwrites X0 (WAR with call 1)
+    Y4 = dg.matmul(Xd, Y1, mode="simt")                      # reads both again
+    torch.cuda.synchronize()
+    x0, w0, w1, w2 = (t.double().numpy() for t in (X0, W[0], W[1], W[2]))
+    y1 = x0 @ w0
+    y2 = y1 @ w1
+    x3 = y2 @ w2
+    y4 = x3 @ y1
+    for got, want, what in [(Y1, y1, "Y1"), (Y2, y2, "Y2"), (Xd, x3, "X overwritten"), (Y4, y4, "Y4")]:
+        err = np.abs(got.cpu().double().numpy() - want).max() / np.abs(want).max()
+        assert err < 1e-5, f"{what}: relative error {err:.2e}"
