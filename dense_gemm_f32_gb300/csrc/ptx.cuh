@@ -115,6 +115,26 @@ __device__ __forceinline__ void bulk_wait_group_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// Named barrier `id` over `count` threads (whole warps).
+template <int ID, int COUNT>
+__device__ __forceinline__ void named_bar_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+
+// Named barrier that also ANDs a predicate over the `count` threads: every
+// thread gets the same answer.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool named_bar_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, o;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred o, %2, %3, q;\n\tselp.u32 %0, 1, 0, o;\n\t}"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u), "n"(ID), "n"(COUNT)
+      : "memory");
+  return r != 0;
+}
+
 // Wait until at most N bulk async-groups of this thread are incomplete.
 template <int N>
 __device__ __forceinline__ void bulk_wait_group() {

@@ -669,9 +669,9 @@ struct Cfg2 {
   static constexpr int THREADS = 32 * (3 + kEpiWarps + kSplitWarps);
   // full, empty, ready (3xTF32), accf[2], acce[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 6;  // + the test-stall barrier
-  // epilogue staging: per epilogue warp two 32 x 32 fp32 chunks (TMA stores)
-  static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;
-  static constexpr int EPI_BYTES = kEpiWarps * 2 * EPI_CHUNK_BYTES;
+  // epilogue staging: two buffers of one 128 x 32 fp32 chunk (one TMA store each)
+  static constexpr int EPI_BUF_BYTES = 32 * kEpiWarps * 32 * 4;
+  static constexpr int EPI_BYTES = 2 * EPI_BUF_BYTES;
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
@@ -684,6 +684,12 @@ struct Cfg2 {
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(kSplitWarp0 == 3 + kEpiWarps, "split warps follow the B producer warp");
 };
+
+// Epilogue pacing of the CTA-pair kernel: chunk c (of 8) of a tile's C waits
+// until c / kPaceParts of the previous accumulator spacing has passed; the
+// spacing is capped at kPaceMaxCycles (about 1 ms), far below the wait limit.
+constexpr int kPaceParts = 12;
+constexpr long long kPaceMaxCycles = 1ll << 21;
 
 enum : int {
   kSite2ProducerEmpty = 0x51,
@@ -935,43 +941,64 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     }
   } else if (warp < 2 + G::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
+    // The four epilogue warps work in step (named barrier 1): each 32-column
+    // chunk of this CTA's 128 x 256 accumulator goes out as one 128 x 32 TMA
+    // store, issued by the first epilogue warp.
     const int quarter = warp & 3;
-    int epi_chunk = 0;  // TMA-store chunks issued by this warp
+    const bool issuer = warp == 2 && lane == 0;
+    int epi_chunk = 0;  // TMA-store chunks issued by this CTA's epilogue
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
+    long long t_prev = 0, t_span = 0;
     for (int tile = cluster; tile < num_tiles; tile += clusters) {
       int tm, tn;
       tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
       bool ok = !*abort_flag && mbar_wait(accf_bar(acc), acc_phase);
       if (!ok && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSite2EpiAccFull, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      // one decision for all four warps: they meet at the barrier below
+      if (!named_bar_and<1, 32 * G::kEpiWarps>(ok)) break;
       tc_fence_after();
-      const int row0 = tm * G::BM + (int)rank * G::HM + quarter * 32;
-      const int row = row0 + lane;
+      // Pacing.  Every CTA finishes its tiles at about the same time, and C
+      // written in one burst from all SMs holds up the operand loads of the
+      // next tiles.  The chunks of a tile are therefore spread over the first
+      // 7/12 of the next tile's main loop (its length taken from the spacing
+      // of the last two accumulators, capped), which the second accumulator
+      // leaves room for.  The first tile is not paced (no spacing known yet),
+      // nor the last one (nothing left to overlap with).
+      const long long t_acc = clock64();
+      if (t_prev) t_span = min(t_acc - t_prev, kPaceMaxCycles);
+      t_prev = t_acc;
+      const bool pace = t_span > 0 && tile + clusters < num_tiles;
+      const int row0 = tm * G::BM + (int)rank * G::HM;  // this CTA's first row of C
+      const int row = row0 + quarter * 32 + lane;
       float *crow = C + (int64_t)row * ldc;
       const uint32_t t_row =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * G::BN);
 #pragma unroll 1
       for (int c0 = 0; c0 < G::BN; c0 += 32) {
+        if (pace && c0 > 0) {
+          const long long due = t_acc + t_span * (c0 / 32) / kPaceParts;
+          while (clock64() < due) __nanosleep(100);
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
         tmem_wait_ld();
         const int col = tn * G::BN + c0;
         if (c_tma && col + 32 <= N) {
-          // Stage the warp's 32 x 32 chunk (row = lane) in 128B-swizzled shared
-          // memory and write it with one TMA store (full lines; rows past M are
-          // dropped by the hardware).  Only chunks wholly inside N go this way:
-          // at the inner edge a TMA store writes whole 16-byte granules, which
-          // would touch the ldc gap when N is not a multiple of 4.  Two buffers
-          // per warp; before one is refilled, the store issued from it two
-          // chunks ago must have read it.
-          const uint32_t buf = epi_base + (uint32_t)(((warp - 2) * 2 + (epi_chunk & 1)) *
-                                                     G::EPI_CHUNK_BYTES);
-          if (lane == 0 && epi_chunk >= 2) bulk_wait_group_read<1>();
-          __syncwarp();
-          const uint32_t row_addr = buf + (uint32_t)(lane * 128);
+          // Each warp stages its 32 rows (row = lane) of the chunk in
+          // 128B-swizzled shared memory; the 128-row box goes out in one TMA
+          // store (full lines; rows past M are dropped by the hardware).  Only
+          // chunks wholly inside N go this way: at the inner edge a TMA store
+          // writes whole 16-byte granules, which would touch the ldc gap when N
+          // is not a multiple of 4.  The condition is the same in all four
+          // warps.  Two buffers; before one is refilled, the store issued from
+          // it two chunks ago must have read it.
+          const uint32_t buf = epi_base + (uint32_t)((epi_chunk & 1) * G::EPI_BUF_BYTES);
+          if (issuer && epi_chunk >= 2) bulk_wait_group_read<1>();
+          named_bar_sync<1, 32 * G::kEpiWarps>();
+          const uint32_t row_addr = buf + (uint32_t)(quarter * 32 * 128 + lane * 128);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t dst = row_addr + (uint32_t)(((c ^ (lane & 7)) << 4));
@@ -980,8 +1007,8 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
                          : "memory");
           }
           fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
+          named_bar_sync<1, 32 * G::kEpiWarps>();
+          if (issuer) {
             // A box wholly outside C is not issued; a (possibly empty) group
             // is committed for every chunk so that "at most one group still
             // reading" always refers to the other buffer.
@@ -1003,7 +1030,7 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_group<0>();  // every TMA store of this warp complete
+    if (issuer) bulk_wait_group<0>();  // every TMA store of this CTA complete
     __syncwarp();
   } else if constexpr (G::kSplit) {
     // ------------------------------------- 3xTF32 split warps (both CTAs)
@@ -1281,7 +1308,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   // C through TMA stores when its rows start on 16-byte boundaries.
   memset(&tc, 0, sizeof(tc));
   const bool c_tma = c_vec && make_map(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32,
-                                       32, CU_TENSOR_MAP_SWIZZLE_128B);
+                                       G::HM, CU_TENSOR_MAP_SWIZZLE_128B);
   auto kern = tc2_gemm_kernel<KIND, AT, BT>;
   static std::atomic<int> max_clusters[64] = {};
   int dev = 0;
