@@ -138,10 +138,11 @@ int validate(int M, int N, int K, bool a_t, bool b_t, const void *A, int lda, co
 // ------------------------------------------------------------------------
 // Scratch: a library-owned stream-ordered memory pool per device.  Freed
 // scratch stays reserved in the pool (up to kPoolKeepBytes) so that the next
-// call's allocation is a pool hit instead of a trip to the driver.
+// call's allocation is a pool hit instead of a trip to the driver; 1 GiB
+// holds the lo parts of 3xTF32 operands up to 16384 x 8192 each.
 namespace dg {
 namespace {
-constexpr uint64_t kPoolKeepBytes = 256ull << 20;
+constexpr uint64_t kPoolKeepBytes = 1ull << 30;
 std::mutex g_pool_mutex;
 cudaMemPool_t g_pools[64] = {};
 }  // namespace
@@ -240,7 +241,7 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
   const int b_rows = b_t ? N : K, b_cols = b_t ? K : N;
   const void *Ause = A, *Buse = B;
   int64_t lda_use = lda, ldb_use = ldb;
-  void *scratch = nullptr;
+  void *scratch = nullptr, *lo_scratch = nullptr;
   const bool a_ok = tma_ok(A, lda, es), b_ok = tma_ok(B, ldb, es);
   cudaError_t e = cudaSuccess;
   if (!a_ok || !b_ok) {
@@ -264,11 +265,36 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
       ldb_use = ldb2;
     }
   }
-  e = dg::launch_tc(kind, a_t, b_t, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
-                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
+  {
+    // 3xTF32 on the CTA-pair kernel: the split pre-pass writes lo(A) and
+    // lo(B) into scratch with the operands' own leading dimensions.  If that
+    // scratch cannot be had, the single-CTA kernel splits in shared memory.
+    const void *Alo = nullptr, *Blo = nullptr;
+    if (kind == dg::TcKind::k3xTF32 && dg::tc_use_pair(M, N, num_sms)) {
+      const size_t al = (size_t)(((int64_t)a_rows * lda_use * 4 + 255) / 256 * 256);
+      const size_t bl = (size_t)(((int64_t)b_rows * ldb_use * 4 + 255) / 256 * 256);
+      if (dg::scratch_alloc(&lo_scratch, al + bl, stream) == cudaSuccess) {
+        char *l = static_cast<char *>(lo_scratch);
+        e = dg::launch_split_lo(static_cast<const float *>(Ause), lda_use,
+                                reinterpret_cast<float *>(l), a_rows, a_cols,
+                                static_cast<const float *>(Buse), ldb_use,
+                                reinterpret_cast<float *>(l + al), b_rows, b_cols, num_sms,
+                                stream);
+        if (e != cudaSuccess) goto done;
+        Alo = l;
+        Blo = l + al;
+      } else {
+        lo_scratch = nullptr;
+        (void)cudaGetLastError();  // the failed allocation is not this call's error
+      }
+    }
+    e = dg::launch_tc(kind, a_t, b_t, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
+                      aligned(C, 16) && (ldc % 4) == 0, num_sms, stream, Alo, Blo);
+  }
 done:
-  if (scratch != nullptr) {
-    cudaError_t e2 = dg::scratch_free(scratch, stream);
+  for (void *p : {lo_scratch, scratch}) {
+    if (p == nullptr) continue;
+    cudaError_t e2 = dg::scratch_free(p, stream);
     if (e == cudaSuccess && e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
   }
   return after_launch(e, "tensor-core GEMM launch");
@@ -307,12 +333,14 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
   int64_t lda_use = lda, ldb_use = ldb;
   const bool a_ok = tma_ok(A, lda, es), b_ok = tma_ok(B, ldb, es);
   cudaError_t e = cudaSuccess;
+  uint64_t used = 0;  // bytes of the fixed scratch taken by re-pitched copies
   if (!a_ok || !b_ok) {
     const int64_t lda2 = (K + pitch_elems - 1) / pitch_elems * pitch_elems;
     const int64_t ldb2 = (N + pitch_elems - 1) / pitch_elems * pitch_elems;
     const uint64_t a_bytes = a_ok ? 0 : ((uint64_t)M * lda2 * es + 255) / 256 * 256;
     const uint64_t b_bytes = b_ok ? 0 : ((uint64_t)K * ldb2 * es + 255) / 256 * 256;
     if (a_bytes + b_bytes > (uint64_t)DGEMM_NOALLOC_SCRATCH_BYTES) return DGEMM_ERR_SCRATCH_LIMIT;
+    used = a_bytes + b_bytes;
     void *base = nullptr;
     const int st = noalloc_scratch(dev, &base);
     if (st != DGEMM_OK) return st;
@@ -330,8 +358,27 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
       ldb_use = ldb2;
     }
   }
+  // 3xTF32 on the CTA-pair kernel when the lo parts fit in the rest of the
+  // fixed scratch; otherwise the single-CTA kernel splits in shared memory.
+  const void *Alo = nullptr, *Blo = nullptr;
+  if (kind == dg::TcKind::k3xTF32 && dg::tc_use_pair(M, N, num_sms)) {
+    const uint64_t al = ((uint64_t)M * lda_use * 4 + 255) / 256 * 256;
+    const uint64_t bl = ((uint64_t)K * ldb_use * 4 + 255) / 256 * 256;
+    if (used + al + bl <= (uint64_t)DGEMM_NOALLOC_SCRATCH_BYTES) {
+      void *base = nullptr;
+      const int st = noalloc_scratch(dev, &base);
+      if (st != DGEMM_OK) return st;
+      char *l = static_cast<char *>(base) + used;
+      e = dg::launch_split_lo(static_cast<const float *>(Ause), lda_use,
+                              reinterpret_cast<float *>(l), M, K, static_cast<const float *>(Buse),
+                              ldb_use, reinterpret_cast<float *>(l + al), K, N, num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "split pre-pass launch (no-alloc)");
+      Alo = l;
+      Blo = l + al;
+    }
+  }
   e = dg::launch_tc(kind, false, false, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc,
-                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream);
+                    aligned(C, 16) && (ldc % 4) == 0, num_sms, stream, Alo, Blo);
   return after_launch(e, "tensor-core GEMM launch (no-alloc)");
 }
 

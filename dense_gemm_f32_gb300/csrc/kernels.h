@@ -41,16 +41,21 @@ enum class TcKind { kTF32 = 0, k3xTF32 = 1, kBF16 = 2, kF16 = 3, kE4M3 = 4, kE5M
 // bytes).  C fp32 row-major.
 // Problems with few tiles split them along K across thread-block clusters;
 // nothing is allocated.
+// 3xTF32 on the CTA-pair kernel reads the lo parts of A and B from A_lo and
+// B_lo (launch_split_lo, same leading dimensions); with A_lo or B_lo null
+// it runs on the single-CTA kernel, which splits in shared memory.
 cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
                       int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                      int num_sms, cudaStream_t stream);
+                      int num_sms, cudaStream_t stream, const void *A_lo = nullptr,
+                      const void *B_lo = nullptr);
 
 // One operand layout each (unit u = 2 * a_t + b_t, one translation unit each);
 // `watchdog` is the device address of the watchdog word.
 #define DG_DECLARE_TC_UNIT(u)                                                                 \
   cudaError_t launch_tc_unit_##u(TcKind kind, int M, int N, int K, const void *A, int64_t lda, \
                                  const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec, \
-                                 int num_sms, int *watchdog, cudaStream_t stream);
+                                 int num_sms, int *watchdog, cudaStream_t stream,              \
+                                 const void *A_lo, const void *B_lo);
 DG_DECLARE_TC_UNIT(0)
 DG_DECLARE_TC_UNIT(1)
 DG_DECLARE_TC_UNIT(2)
@@ -69,8 +74,23 @@ cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t l
 cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
                            int cols, int elem_bytes, int num_sms, cudaStream_t stream);
 
+// 3xTF32 split pre-pass: A_lo = lo(A) (a_rows x a_cols, leading dimension
+// lda) and B_lo = lo(B) likewise, lo(x) = x - trunc_tf32(x) rounded to TF32
+// (0 for infinities and NaNs), in one launch.  All four bases 16-byte aligned,
+// lda and ldb multiples of 4.
+cudaError_t launch_split_lo(const float *A, int64_t lda, float *A_lo, int a_rows, int a_cols,
+                            const float *B, int64_t ldb, float *B_lo, int b_rows, int b_cols,
+                            int num_sms, cudaStream_t stream);
+
+// Whether a tensor-core GEMM of M x N runs on the CTA-pair kernel (256 x 256
+// tiles) rather than the single-CTA kernel: once there are enough pair tiles
+// to occupy at least a quarter of the SMs, since it has half as many tiles.
+// DGEMM_TC_PAIR=0 / =1 forces one of them (read on every call, for tests and
+// tuning).
+bool tc_use_pair(int M, int N, int num_sms);
+
 // Stream-ordered scratch from the library's memory pool on the current device
-// (freed scratch stays reserved in the pool for reuse, up to 256 MiB).
+// (freed scratch stays reserved in the pool for reuse, up to 1 GiB).
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);
 cudaError_t scratch_free(void *ptr, cudaStream_t stream);
 

@@ -1,6 +1,6 @@
 // staging.cu -- re-pitching of operands the tensor-memory accelerator cannot
 // address, and the transpose of 8-bit operands into the K-major layout the
-// tensor cores read them in.
+// tensor cores read them in, and the split pre-pass of 3xTF32.
 //
 // TMA reads a matrix only if its base is 16-byte aligned and its row pitch is
 // a multiple of 16 bytes ("第八课：GPU 如何完成矩阵乘法" section 二十二 lists
@@ -13,6 +13,7 @@
 
 #include "kernels.h"
 #include "launch.cuh"
+#include "tf32_split.cuh"
 
 namespace dg {
 namespace {
@@ -111,6 +112,44 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// lo part of the 3xTF32 split of one operand: L[r][c] = split_lo(X[r][c])
+// for r < rows, c < cols, with the same leading dimension (a multiple of 4,
+// both bases 16-byte aligned: the operand already meets the TMA rules).
+struct SplitOperand {
+  const uint32_t *x;
+  uint32_t *lo;
+  int64_t ld;
+  int rows, cols;
+};
+
+// Blocks [0, blocks_a) split operand a, the rest operand b.  Within an
+// operand: rows along blockIdx (grid-stride), 16-byte chunks of a row along
+// the threads; the chunk at the end of a row that is not whole goes element by
+// element (the row may end there in memory).
+__global__ void split_lo_kernel(SplitOperand a, SplitOperand b, int blocks_a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const bool first = (int)blockIdx.x < blocks_a;
+  const SplitOperand op = first ? a : b;
+  const int nblocks = first ? blocks_a : (int)gridDim.x - blocks_a;
+  const int bid = first ? (int)blockIdx.x : (int)blockIdx.x - blocks_a;
+  const int chunks = (op.cols + 3) / 4;
+  const int whole = op.cols / 4;
+  for (int r = bid; r < op.rows; r += nblocks) {
+    const uint32_t *xr = op.x + (int64_t)r * op.ld;
+    uint32_t *lr = op.lo + (int64_t)r * op.ld;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      if (c < whole) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + c);
+        reinterpret_cast<uint4 *>(lr)[c] = make_uint4(split_lo_tf32(v.x), split_lo_tf32(v.y),
+                                                      split_lo_tf32(v.z), split_lo_tf32(v.w));
+      } else {
+        for (int j = 4 * c; j < op.cols; ++j) lr[j] = split_lo_tf32(__ldg(xr + j));
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
@@ -143,6 +182,29 @@ cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd,
                                       lds * elem_bytes, static_cast<uint8_t *>(dst),
                                       ldd * elem_bytes, rows, (int64_t)cols * elem_bytes,
                                       elem_bytes);
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+cudaError_t launch_split_lo(const float *A, int64_t lda, float *A_lo, int a_rows, int a_cols,
+                            const float *B, int64_t ldb, float *B_lo, int b_rows, int b_cols,
+                            int num_sms, cudaStream_t stream) {
+  if ((a_rows <= 0 || a_cols <= 0) && (b_rows <= 0 || b_cols <= 0)) return cudaSuccess;
+  const SplitOperand a = {reinterpret_cast<const uint32_t *>(A), reinterpret_cast<uint32_t *>(A_lo),
+                          lda, a_cols > 0 ? a_rows : 0, a_cols};
+  const SplitOperand b = {reinterpret_cast<const uint32_t *>(B), reinterpret_cast<uint32_t *>(B_lo),
+                          ldb, b_cols > 0 ? b_rows : 0, b_cols};
+  // blocks in proportion to the bytes of each operand, 8 per SM in all
+  const double ea = (double)a.rows * a_cols, eb = (double)b.rows * b_cols;
+  const int total = num_sms * 8;
+  int ba = (int)(total * ea / (ea + eb) + 0.5);
+  if (ba < 1 && a.rows > 0) ba = 1;
+  if (ba > a.rows) ba = a.rows;
+  int bb = total - ba;
+  if (bb < 1 && b.rows > 0) bb = 1;
+  if (bb > b.rows) bb = b.rows;
+  const cudaError_t e = launch_kernel(split_lo_kernel, dim3((unsigned)(ba + bb)), dim3(256), 0,
+                                      stream, 1, a, b, ba);
   if (e == cudaSuccess) count_launch();
   return e;
 }

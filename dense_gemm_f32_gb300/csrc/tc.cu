@@ -46,6 +46,7 @@
 #include "kernels.h"
 #include "launch.cuh"
 #include "ptx.cuh"
+#include "tf32_split.cuh"
 
 // This file is compiled once per operand layout: DGEMM_TC_UNIT = 2 * AT + BT
 // selects which kernels one translation unit instantiates (AT: A stored
@@ -206,33 +207,6 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
 __device__ __forceinline__ void watchdog_trip(int *watchdog, int site, volatile int *abort_flag) {
   atomicCAS(watchdog, 0, site);
   *abort_flag = 1;
-}
-
-// 3xTF32 split of x = hi + lo.  The tensor core reads an fp32 operand at TF32
-// precision by dropping its low 13 mantissa bits (truncation; pinned by a GPU
-// test), so the raw fp32 tile itself serves as hi = trunc_tf32(x) and only lo
-// is written: lo = x - hi, exact in fp32, rounded to TF32 (nearest, ties
-// away).  The dropped lo*lo term and the rounding of lo are each below
-// 2^-20 |x y| per product.  Infinities and NaNs have no low part (x - x
-// would be NaN and turn an infinite result into NaN): their lo is 0 and the
-// raw value carries them, as in the plain TF32 product.
-__device__ __forceinline__ uint32_t split_lo_tf32(uint32_t xbits) {
-  const float r = __uint_as_float(xbits) - __uint_as_float(xbits & 0xFFFFE000u);
-  uint32_t l;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
-  return (xbits & 0x7F800000u) == 0x7F800000u ? 0u : l;
-}
-
-// The split's fast path: the same lo without the infinity / NaN test, and
-// `seen` becomes NaN if any x was infinite or NaN (x - x is NaN then), one
-// max.NaN per element; the caller redoes its elements with split_lo_tf32
-// in that (rare) case.
-__device__ __forceinline__ uint32_t split_lo_tf32_fast(uint32_t xbits, float &seen) {
-  const float r = __uint_as_float(xbits) - __uint_as_float(xbits & 0xFFFFE000u);
-  asm("max.NaN.f32 %0, %0, %1;" : "+f"(seen) : "f"(r));
-  uint32_t l;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
-  return l;
 }
 
 template <TcKind KIND, int BN, bool AT, bool BT>
@@ -657,7 +631,7 @@ struct Cfg2 {
   static constexpr int B_BOXES = BT ? 1 : HN / BOX;
   static constexpr int B_BOX_BYTES = BT ? B_BYTES : BK * 128;
   static constexpr int RAW_BYTES = A_BYTES + B_BYTES;                // per CTA, per stage
-  static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);   // + lo copies (3xTF32)
+  static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);   // + lo parts (3xTF32)
   static constexpr int STAGES = 196608 / STAGE_BYTES;
   static constexpr int TMEM_COLS = 512;                   // two 256-column accumulators
   static constexpr int kEpiWarps = 4;
@@ -665,10 +639,9 @@ struct Cfg2 {
   // instruction takes ~70 cycles to issue whatever its box size, and one
   // thread issuing every box of a stage fell behind the MMAs.
   static constexpr int kProdBWarp = 2 + kEpiWarps;
-  static constexpr int kSplitWarp0 = kProdBWarp + 1, kSplitWarps = kSplit ? 8 : 0;
-  static constexpr int THREADS = 32 * (3 + kEpiWarps + kSplitWarps);
-  // full, empty, ready (3xTF32), accf[2], acce[2], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 6;  // + the test-stall barrier
+  static constexpr int THREADS = 32 * (3 + kEpiWarps);
+  // full, empty, accf[2], acce[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 6;  // + the test-stall barrier
   // epilogue staging: two buffers of one 128 x 32 fp32 chunk (one TMA store each)
   static constexpr int EPI_BUF_BYTES = 32 * kEpiWarps * 32 * 4;
   static constexpr int EPI_BYTES = 2 * EPI_BUF_BYTES;
@@ -682,7 +655,6 @@ struct Cfg2 {
                                     ((AT ? 1u : 0u) << 15) | ((BT ? 0u : 1u) << 16) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
-  static_assert(kSplitWarp0 == 3 + kEpiWarps, "split warps follow the B producer warp");
 };
 
 // Epilogue pacing of the CTA-pair kernel: chunk c (of 8) of a tile's C waits
@@ -699,7 +671,6 @@ enum : int {
   kSite2MmaDrain = 0x63,
   kSite2MmaTail = 0x64,
   kSite2EpiAccFull = 0x71,
-  kSite2SplitFull = 0x81,
   kSite2TestStall = 0x66,  // DGEMM_TC_TEST_STALL: the MMA thread's test wait ran out
 };
 
@@ -707,7 +678,9 @@ template <TcKind KIND, bool AT, bool BT>
 __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
-                    const __grid_constant__ CUtensorMap tmap_c, float *__restrict__ C, int M,
+                    const __grid_constant__ CUtensorMap tmap_c,
+                    const __grid_constant__ CUtensorMap tmap_al,
+                    const __grid_constant__ CUtensorMap tmap_bl, float *__restrict__ C, int M,
                     int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog,
                     int mn3d, int stall) {
   using G = Cfg2<KIND, AT, BT>;
@@ -721,11 +694,10 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
   const uint32_t bars = epi_base + G::EPI_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (G::STAGES + s); };
-  auto ready_bar = [&](int s) { return bars + 8u * (2 * G::STAGES + s); };
-  auto accf_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
-  const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
-  const uint32_t stall_bar = bars + 8u * (3 * G::STAGES + 5);  // nothing ever arrives here
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * G::STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * G::STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * G::STAGES + 4);
+  const uint32_t stall_bar = bars + 8u * (2 * G::STAGES + 5);  // nothing ever arrives here
   uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::EPI_BYTES + G::NUM_BARS * 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
@@ -747,7 +719,6 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     for (int s = 0; s < G::STAGES; ++s) {
       mbar_init(full_bar(s), 2);  // one arrival per producer thread
       mbar_init(empty_bar(s), 1);
-      mbar_init(ready_bar(s), G::kSplit ? 2 * G::kSplitWarps : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -762,6 +733,10 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
     if (c_tma) tma_prefetch_desc(&tmap_c);
+    if constexpr (G::kSplit) {
+      tma_prefetch_desc(&tmap_al);
+      tma_prefetch_desc(&tmap_bl);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(tmem_slot)), G::TMEM_COLS);
@@ -779,12 +754,14 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     // ----------------------------------------------------------- producers
     // warp 0 loads this CTA's part of op(A), warp kProdBWarp its part of
     // op(B); each arrives once per stage on the full barrier with its bytes.
+    // 3xTF32: each also loads the lo part of its operand (written by the
+    // split pre-pass, same geometry) into the stage's lo area.
     if (lane == 0) {
       const bool is_a = warp == 0;
-      const uint32_t bytes = is_a ? (uint32_t)G::A_BYTES : (uint32_t)G::B_BYTES;
-      // 3xTF32: each CTA's split warps wait on its own full barrier; else both
-      // CTAs' halves signal the even CTA's full barrier (stage s at +8 s).
-      const uint32_t fb0 = G::kSplit ? full_bar(0) : mapa_shared(full_bar(0), 0);
+      const uint32_t bytes =
+          (is_a ? (uint32_t)G::A_BYTES : (uint32_t)G::B_BYTES) * (G::kSplit ? 2u : 1u);
+      // Both CTAs' halves signal the even CTA's full barrier (stage s at +8 s).
+      const uint32_t fb0 = mapa_shared(full_bar(0), 0);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -809,39 +786,32 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
           // takes the arrival off the path from a free stage to its loads.
           // An MN-major operand with a 3-D map comes in one instruction.
           const bool one3d = is_a ? (AT && (mn3d & kA3d)) : (!BT && (mn3d & kB3d));
-          if (one3d) {
-            const uint32_t dst = is_a ? a_tile(stage) : b_tile(stage);
-            const CUtensorMap *map = is_a ? &tmap_a : &tmap_b;
-            const int z = (is_a ? m0 : n0) / G::BOX;
-            if constexpr (G::kSplit)
-              tma_load_3d(dst, map, fb, 0, kb * G::BK, z);
-            else
+#pragma unroll
+          for (int part = 0; part < (G::kSplit ? 2 : 1); ++part) {  // raw, then lo
+            const uint32_t lo_off = part ? (uint32_t)G::RAW_BYTES : 0u;
+            if (one3d) {
+              const uint32_t dst = (is_a ? a_tile(stage) : b_tile(stage)) + lo_off;
+              const CUtensorMap *map =
+                  is_a ? (part ? &tmap_al : &tmap_a) : (part ? &tmap_bl : &tmap_b);
+              const int z = (is_a ? m0 : n0) / G::BOX;
               tma_load_3d_pair(dst, map, fb, 0, kb * G::BK, z);
-          } else if (is_a) {
+            } else if (is_a) {
 #pragma unroll
-            for (int j = 0; j < G::A_BOXES; ++j) {
-              const uint32_t dst = a_tile(stage) + j * G::A_BOX_BYTES;
-              const int x = AT ? m0 + j * G::BOX : kb * G::BK, y = AT ? kb * G::BK : m0;
-              if constexpr (G::kSplit)
-                tma_load_2d(dst, &tmap_a, fb, x, y);
-              else
-                tma_load_2d_pair(dst, &tmap_a, fb, x, y);
-            }
-          } else {
+              for (int j = 0; j < G::A_BOXES; ++j) {
+                const uint32_t dst = a_tile(stage) + lo_off + j * G::A_BOX_BYTES;
+                const int x = AT ? m0 + j * G::BOX : kb * G::BK, y = AT ? kb * G::BK : m0;
+                tma_load_2d_pair(dst, part ? &tmap_al : &tmap_a, fb, x, y);
+              }
+            } else {
 #pragma unroll
-            for (int j = 0; j < G::B_BOXES; ++j) {
-              const uint32_t dst = b_tile(stage) + j * G::B_BOX_BYTES;
-              const int x = BT ? kb * G::BK : n0 + j * G::BOX, y = BT ? n0 : kb * G::BK;
-              if constexpr (G::kSplit)
-                tma_load_2d(dst, &tmap_b, fb, x, y);
-              else
-                tma_load_2d_pair(dst, &tmap_b, fb, x, y);
+              for (int j = 0; j < G::B_BOXES; ++j) {
+                const uint32_t dst = b_tile(stage) + lo_off + j * G::B_BOX_BYTES;
+                const int x = BT ? kb * G::BK : n0 + j * G::BOX, y = BT ? n0 : kb * G::BK;
+                tma_load_2d_pair(dst, part ? &tmap_bl : &tmap_b, fb, x, y);
+              }
             }
           }
-          if (G::kSplit)
-            mbar_arrive_expect_tx(full_bar(stage), bytes);
-          else if (leader)
-            mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * bytes);
           if (++stage == G::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -885,8 +855,9 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * G::BN);
         for (int kb = 0; kb < kblocks; ++kb) {
-          const uint32_t ready = G::kSplit ? ready_bar(stage) : full_bar(stage);
-          if (!mbar_try_wait(ready, phase) && (*abort_flag || !mbar_wait(ready, phase))) {
+          const bool got = mbar_try_wait(full_bar(stage), phase) ||
+                           (!*abort_flag && mbar_wait(full_bar(stage), phase));
+          if (!got) {
             if (!*abort_flag) watchdog_trip(watchdog, kSite2MmaFull, abort_flag);
             ok = false;
             break;
@@ -1032,55 +1003,6 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
     }
     if (issuer) bulk_wait_group<0>();  // every TMA store of this CTA complete
     __syncwarp();
-  } else if constexpr (G::kSplit) {
-    // ------------------------------------- 3xTF32 split warps (both CTAs)
-    // Write the lo parts of this CTA's staged tiles (the raw tile is hi), then release
-    // the stage on the even CTA's ready barrier (4 warps x 2 CTAs).
-    const int t = threadIdx.x - 32 * G::kSplitWarp0;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int tile = cluster; tile < num_tiles && ok; tile += clusters) {
-      for (int kb = 0; kb < kblocks; ++kb) {
-        bool got = !*abort_flag && mbar_wait(full_bar(stage), phase);
-        if (!got && lane == 0 && !*abort_flag) watchdog_trip(watchdog, kSite2SplitFull, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        uint4 *raw = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES);
-        uint4 *lo = reinterpret_cast<uint4 *>(smem + stage * G::STAGE_BYTES + G::RAW_BYTES);
-        constexpr int kStride = 32 * G::kSplitWarps;
-        constexpr int kIters = G::RAW_BYTES / 16 / kStride;
-        static_assert(kIters % 4 == 0, "the split loop is unrolled by 4");
-        float seen = 0.f;
-#pragma unroll 1
-        for (int it = 0; it < kIters; it += 4) {
-          uint4 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[u] = raw[t + (it + u) * kStride];  // loads first
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            lo[t + (it + u) * kStride] =
-                make_uint4(split_lo_tf32_fast(v[u].x, seen), split_lo_tf32_fast(v[u].y, seen),
-                           split_lo_tf32_fast(v[u].z, seen), split_lo_tf32_fast(v[u].w, seen));
-        }
-        if (seen != seen) {  // an infinity or NaN in this thread's elements
-          for (int i = t; i < G::RAW_BYTES / 16; i += kStride) {
-            const uint4 v = raw[i];
-            lo[i] = make_uint4(split_lo_tf32(v.x), split_lo_tf32(v.y), split_lo_tf32(v.z),
-                               split_lo_tf32(v.w));
-          }
-        }
-        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(ready_bar(stage), 0));
-        if (++stage == G::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -1299,12 +1221,24 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
 template <TcKind KIND, bool AT, bool BT>
 cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const void *B,
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, int *watchdog,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const void *A_lo, const void *B_lo) {
   using G = Cfg2<KIND, AT, BT>;
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tb, tc, tal, tbl;
   int mn3d = 0;
   if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, G::HM, G::HN, &mn3d))
     return cudaErrorInvalidValue;
+  // 3xTF32: maps of the lo parts, the same geometry (and the same choice of
+  // 3-D maps, which the kernel makes once for both)
+  memset(&tal, 0, sizeof(tal));
+  memset(&tbl, 0, sizeof(tbl));
+  if constexpr (G::kSplit) {
+    int mn3d_lo = 0;
+    if (A_lo == nullptr || B_lo == nullptr ||
+        !make_operand_maps<G, KIND>(&tal, &tbl, M, N, K, A_lo, lda, B_lo, ldb, G::HM, G::HN,
+                                    &mn3d_lo) ||
+        mn3d_lo != mn3d)
+      return cudaErrorInvalidValue;
+  }
   // C through TMA stores when its rows start on 16-byte boundaries.
   memset(&tc, 0, sizeof(tc));
   const bool c_tma = c_vec && make_map(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32,
@@ -1339,32 +1273,24 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   e = launch_kernel(kern, dim3(2 * clusters), dim3(G::THREADS), G::SMEM_BYTES, stream, 2u, ta, tb,
-                    tc, C, M, N, K, ldc, c_tma ? 1 : 0, raster_group_m(16), watchdog, mn3d,
-                    test_stall());
+                    tc, tal, tbl, C, M, N, K, ldc, c_tma ? 1 : 0, raster_group_m(16), watchdog,
+                    mn3d, test_stall());
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
 }
 
-// Pair kernel or single-CTA kernel.  DGEMM_TC_PAIR=0 / =1 forces one of them
-// (read on every call, for tests and tuning); by default the pair kernel runs
-// once there are enough 256 x 256 tiles to occupy at least a quarter of the
-// SMs, since it has half as many tiles as the single-CTA kernel.
-bool use_pair(int M, int N, int num_sms) {
-  const char *e = getenv("DGEMM_TC_PAIR");
-  if (e && e[0] == '0') return false;
-  if (e && e[0] == '1') return true;
-  const int64_t pair_tiles = (int64_t)((M + 255) / 256) * ((N + 255) / 256);
-  return pair_tiles * 4 >= num_sms;
-}
-
+// Pair kernel or single-CTA kernel (tc_use_pair); 3xTF32 takes the pair
+// kernel only with the lo parts of A and B at hand.
 template <TcKind KIND, int BN1>
 cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const void *B,
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
-                        int *watchdog, cudaStream_t stream) {
+                        int *watchdog, cudaStream_t stream, const void *A_lo, const void *B_lo) {
   constexpr bool AT = kUnitAT, BT = kUnitBT;
-  if (use_pair(M, N, num_sms))
-    return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream);
+  const bool lo_ok = KIND != TcKind::k3xTF32 || (A_lo != nullptr && B_lo != nullptr);
+  if (lo_ok && tc_use_pair(M, N, num_sms))
+    return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream,
+                                     A_lo, B_lo);
   return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog, stream);
 }
 
@@ -1381,29 +1307,30 @@ __global__ void read_watchdog_kernel(int *out) {
 // This unit's layout: every tensor-core kind with AT = kUnitAT, BT = kUnitBT.
 cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, int64_t lda,
                              const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                             int num_sms, int *watchdog, cudaStream_t stream) {
+                             int num_sms, int *watchdog, cudaStream_t stream, const void *A_lo,
+                             const void *B_lo) {
   switch (kind) {
     case TcKind::kTF32:
       return launch_kind<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, stream);
+                                             watchdog, stream, A_lo, B_lo);
     case TcKind::k3xTF32:
       return launch_kind<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                               watchdog, stream);
+                                               watchdog, stream, A_lo, B_lo);
     case TcKind::kBF16:
       return launch_kind<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, stream);
+                                             watchdog, stream, A_lo, B_lo);
     case TcKind::kF16:
       return launch_kind<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            watchdog, stream);
+                                            watchdog, stream, A_lo, B_lo);
     case TcKind::kE4M3:
     case TcKind::kE5M2:
       // 8-bit operands exist only K-major (A as M x K, B as N x K): this unit
       if constexpr (!kUnitAT && kUnitBT) {
         if (kind == TcKind::kE4M3)
           return launch_kind<TcKind::kE4M3, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
-                                                 num_sms, watchdog, stream);
+                                                 num_sms, watchdog, stream, A_lo, B_lo);
         return launch_kind<TcKind::kE5M2, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                               watchdog, stream);
+                                               watchdog, stream, A_lo, B_lo);
       }
       return cudaErrorInvalidValue;
   }
@@ -1428,21 +1355,33 @@ int *watchdog_address() {
 }
 }  // namespace
 
+bool tc_use_pair(int M, int N, int num_sms) {
+  const char *e = getenv("DGEMM_TC_PAIR");
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  const int64_t pair_tiles = (int64_t)((M + 255) / 256) * ((N + 255) / 256);
+  return pair_tiles * 4 >= num_sms;
+}
+
 cudaError_t launch_tc(TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A,
                       int64_t lda, const void *B, int64_t ldb, float *C, int64_t ldc, bool c_vec,
-                      int num_sms, cudaStream_t stream) {
+                      int num_sms, cudaStream_t stream, const void *A_lo, const void *B_lo) {
   int *wd = watchdog_address();
   if (wd == nullptr) return cudaErrorInvalidSymbol;
   const int unit = (a_t ? 2 : 0) + (b_t ? 1 : 0);
   switch (unit) {
     case 0:
-      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_0(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream,
+                              A_lo, B_lo);
     case 1:
-      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_1(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream,
+                              A_lo, B_lo);
     case 2:
-      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_2(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream,
+                              A_lo, B_lo);
     default:
-      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream);
+      return launch_tc_unit_3(kind, M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, wd, stream,
+                              A_lo, B_lo);
   }
 }
 

@@ -44,9 +44,10 @@
  *     per-thread error string and a per-device watchdog word (see
  *     dgemm_watchdog_status).
  *   - Some paths use temporary device memory (re-pitched operands, the FP32
- *     SIMT path's K-split partials): stream-ordered allocations on `stream` from a memory pool
- *     the library creates per device, which keeps up to 256 MiB of freed
- *     scratch reserved for the next calls.
+ *     SIMT path's K-split partials, the lo parts of 3xTF32 operands):
+ *     stream-ordered allocations on `stream` from a memory pool the library
+ *     creates per device, which keeps up to 1 GiB of freed scratch reserved
+ *     for the next calls.
  */
 #ifndef DGEMM_H
 #define DGEMM_H
@@ -139,6 +140,12 @@ int gemm_f32_simt(int M, int N, int K,
  *                         NaNs propagate as in IEEE arithmetic, except that
  *                         an infinite entry meeting a finite one whose lo is
  *                         exactly 0 adds inf * 0 = NaN to that entry of C.
+ *                         Large problems (those the CTA-pair kernel takes)
+ *                         first write lo(A) and lo(B) to scratch the size of
+ *                         A and B, one extra kernel; if that scratch cannot
+ *                         be allocated, the single-CTA kernel splits the
+ *                         staged tiles in shared memory instead (same result,
+ *                         slower).
  * Argument layout as gemm_f32_simt.  Unknown mode: DGEMM_ERR_UNSUPPORTED.
  */
 int gemm_f32_tc(int mode, int M, int N, int K,
@@ -187,6 +194,9 @@ int gemm_bf16_tc(int M, int N, int K,
  *     each copy rounded up to 256 bytes) must fit in 16 MiB; otherwise the
  *     call returns DGEMM_ERR_SCRATCH_LIMIT and launches nothing.  Operands
  *     that need no re-pitch use no scratch, at any size.
+ *   - 3xTF32 writes the lo parts of A and B into the rest of the array when
+ *     they fit there; larger problems run on the single-CTA kernel, which
+ *     needs no scratch for the split.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins on the device.
