@@ -135,7 +135,7 @@ def kernel_name(mode, M, N, num_sms):
 
 def source_sha(mode):
     csrc = os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc")
-    files = ["simt.cu"] if mode == "simt" else ["tc.cu", "ptx.cuh"]
+    files = ["simt.cu"] if mode == "simt" else ["tc.cu", "ptx.cuh", "tf32_split.cuh"]
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:

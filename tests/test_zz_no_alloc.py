@@ -103,3 +103,27 @@ def test_rejects_operands_beyond_the_scratch():
     assert st == dg.ERR_SCRATCH_LIMIT
     assert "16 MiB" in dg.dgemm_status_string(st)
     assert dg.dgemm_kernel_launches() == n0
+
+
+@pytest.mark.parametrize("K, launches", [(512, 2), (2048, 1)])
+def test_3xtf32_lo_parts_in_the_fixed_scratch(K, launches):
+    """3xTF32 on a problem the CTA-pair kernel takes (2048 x 2048): with
+    K = 512 the lo parts of A and B (8 MiB) fit in the fixed scratch, so the
+    split pre-pass writes them there and the pair kernel loads them (two
+    launches); with K = 2048 (32 MiB) they do not, and the single-CTA kernel
+    splits in shared memory (one launch).  Both match gemm_f32_tc."""
+    M = N = 2048
+    A, B = inputs.make_random(M, N, K, seed=K, dist="normal")
+    Ad, Bd = A.cuda(), B.cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    C = torch.full((M, N), float("nan"), device="cuda")
+    torch.cuda.synchronize()
+    n0 = dg.dgemm_kernel_launches()
+    assert _call(dg.gemm_f32_tc_noalloc, "3xtf32", Ad, Bd, C, stream) == dg.OK
+    assert dg.dgemm_kernel_launches() - n0 == launches
+    ref, new = _pair("3xtf32", Ad, Bd)
+    S = _s(A, B)
+    err = np.abs(new.astype(np.float64) - ref.astype(np.float64))
+    assert np.all(err <= gu.TOL["3xtf32"] * S)
+    assert np.array_equal(C.cpu().numpy(), new)
+    gu.check_watchdog()
