@@ -481,9 +481,11 @@ def cublas_same_run(mode, Ad, Bd, device, steps=10):
         return None
 
 
-def time_graph(mode, Ad, Bd, C, device, calls=20, replays=5):
+def time_graph(mode, Ad, Bd, C, device, calls=20, replays=7):
     """Device time per call of `calls` back-to-back calls captured in one CUDA
-    graph (no host launch gaps; L2 warm after the first call)."""
+    graph (no host launch gaps; L2 warm after the first call): the median over
+    `replays` replays, each timed by its own event pair, so that one replay
+    caught in a clock dip does not move the figure."""
     import torch
 
     import dense_gemm_f32_gb300 as dg
@@ -498,14 +500,15 @@ def time_graph(mode, Ad, Bd, C, device, calls=20, replays=5):
                 dg.matmul(Ad, Bd, mode=mode, out=C)
     g.replay()
     torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     cur = torch.cuda.current_stream(device)
-    e0.record(cur)
-    for _ in range(replays):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+    ev[0].record(cur)
+    for i in range(replays):
         g.replay()
-    e1.record(cur)
+        ev[i + 1].record(cur)
     torch.cuda.synchronize(device)
-    return e0.elapsed_time(e1) * 1e3 / (calls * replays)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(replays)]
+    return statistics.median(per) * 1e3 / calls
 
 
 SMALL_MODES = ("simt", "tf32", "3xtf32", "bf16", "fp16", "e4m3", "e5m2")
