@@ -25,6 +25,10 @@
 //    of A and B are re-read from L2 instead of HBM.
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     const float *parts0 = work + slot * (BM * BN);
     constexpr int Q = BN / 4;                         // float4s per tile row
     constexpr int V = BM * Q / G::THREADS;            // float4s per thread
-    constexpr int CH = 16;
+    constexpr int CH = V < 16 ? V : 16;
     static_assert(V % CH == 0, "whole batches");
 #pragma unroll 1
     for (int c0 = 0; c0 < V; c0 += CH) {
@@ -423,6 +427,39 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   }
 }
 
+// Clusters of `size` CTAs of `kern` (threads, smem bytes each) that can be
+// resident at once on device `dev`; 0 if none.  Cached per kernel, device
+// and size.
+int simt_active_clusters(const void *kern, int threads, int smem, int dev, int size) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, int, int>, int> cache;
+  const auto key = std::make_tuple(kern, dev, size);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)size, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 0) {
+    cudaGetLastError();  // not sticky; treat as "does not fit"
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
+}
+
 template <class G, bool AT, bool BT>
 cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, const float *B,
                             int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
@@ -456,10 +493,23 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   unsigned int *counters = nullptr;
   void *scratch = nullptr;
   cudaError_t e = cudaSuccess;
+  int cparts = 0;  // cluster size for the all-split case, if its clusters fit at once
   if (parts > 1 && rem == tiles) {
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (int p = parts; p >= 2 && cparts == 0; --p)
+      if (tiles <= simt_active_clusters(reinterpret_cast<const void *>(kern), G::THREADS,
+                                        G::SMEM_CLUSTER, dev, p))
+        cparts = p;
+  }
+  if (cparts > 1) {
     // Every tile is split (a small problem): the parts of a tile run as one
     // cluster and add their partials through distributed shared memory; no
-    // scratch, no second pass.
+    // scratch, no second pass.  Only cluster sizes whose clusters are all
+    // resident at once are used: a cluster that waits for a second wave
+    // doubles the time.
+    parts = cparts;
     return launch_kernel(kern, dim3((unsigned)(tiles * parts)), dim3(G::THREADS), G::SMEM_CLUSTER,
                          stream, (unsigned)parts, M, N, K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0,
                          0, parts, nullptr, nullptr, 1);
@@ -507,11 +557,37 @@ __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ld
 #define DGEMM_SIMT_CFG 128, 256, 16, 2, 4, 8, 1
 #endif
 using SimtShipped = SimtCfg<DGEMM_SIMT_CFG>;
+// Small problems: 64 x 64 x 16 block tiles, 128 threads as 2 x 2 warps of
+// 32 x 32, a 4 x 8 register tile per thread, up to 4 CTAs per SM.  At 64^3
+// the shipped 128 x 256 tile computes eight times the useful work on one SM.
+using SimtSmall = SimtCfg<64, 64, 16, 2, 2, 8, 4>;
+
+// The small configuration runs when the shipped tiles are fewer than an
+// eighth of the SMs (the K-split cannot make up for that: 512^3 has 8 tiles)
+// or when a third or more of their area would be padding (M or N well below
+// a multiple of 128 or 256: 64 x 4096 x 4096 pads half of each tile).
+// Measured on GB300 with the K-split on both: small ahead 1.3x at 512^3,
+// 1.9x at 64 x 4096 x 4096 and 2.8x at 4096 x 64 x 4096; shipped ahead
+// 1.2-1.4x at 1024^3, 1000 x 1013 x 997, 1536^3 and 256 x 8192 x 1024, and
+// 1.05x at 3000 x 200 x 2000 (a quarter padding).  DGEMM_SIMT_SMALL=0 / =1
+// forces one of them (read on every call, for tests and tuning).
+static bool simt_use_small(int M, int N, int num_sms) {
+  const char *e = getenv("DGEMM_SIMT_SMALL");
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  const int64_t tm = (M + SimtShipped::BM - 1) / SimtShipped::BM;
+  const int64_t tn = (N + SimtShipped::BN - 1) / SimtShipped::BN;
+  const double padded = (double)(tm * SimtShipped::BM) * (double)(tn * SimtShipped::BN);
+  return tm * tn * 8 < num_sms || padded >= 1.5 * (double)M * (double)N;
+}
 
 // This unit's operand layout.
 cudaError_t DG_SIMT_UNIT_LAUNCHER(int M, int N, int K, const float *A, int64_t lda,
                                   const float *B, int64_t ldb, float *C, int64_t ldc, bool ab_vec,
                                   bool c_vec, int num_sms, cudaStream_t stream) {
+  if (simt_use_small(M, N, num_sms))
+    return launch_simt_cfg<SimtSmall, kUnitAT, kUnitBT>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
+                                                        c_vec, num_sms, stream);
   return launch_simt_cfg<SimtShipped, kUnitAT, kUnitBT>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
                                                         c_vec, num_sms, stream);
 }
