@@ -16,7 +16,9 @@
 //    operand, warps 0 and 6), warp 1 issues tcgen05.mma (one thread) and owns
 //    the TMEM allocation, warps 2-5 drain the accumulator (tcgen05.ld ->
 //    registers -> global, or shared memory and TMA stores).  For 3xTF32 the
-//    remaining warps split each staged fp32 tile into hi and lo TF32 parts.
+//    single-CTA kernel's remaining warps split each staged fp32 tile into hi
+//    and lo TF32 parts; the pair kernel loads lo parts that a pre-pass wrote
+//    (staging.cu: split_lo_kernel) next to the raw tiles.
 //  * Operands: A (M x K, K contiguous) is K-major, B (K x N, N contiguous) is
 //    MN-major (either may be stored transposed instead); they arrive by TMA
 //    boxes of one 128-byte swizzle row width into 128B-swizzled shared
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
 }
 
 // ===================================================================
-// CTA-pair variant (cta_group::2) for TF32 and BF16.
+// CTA-pair variant (cta_group::2), every operand kind.
 //
 // A cluster of two CTAs on two SMs computes a 256 x 256 tile.  CTA r loads
 // rows [128 r, 128 r + 128) of the A panel and columns [128 r, 128 r + 128)
@@ -597,8 +599,13 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
 //    producer posts the expected bytes of both halves.
 //  * The MMA thread's commits arrive on the barrier at the same offset in
 //    both CTAs (multicast): stage-free and accumulator-ready.
-//  * Each CTA's epilogue reads its own TMEM rows; the odd CTA's epilogue
-//    releases the accumulator on the even CTA's barrier.
+//  * Each CTA's epilogue reads its own TMEM rows and writes them with one
+//    128-row TMA store per 32-column chunk, paced over the next tile's main
+//    loop; the odd CTA's epilogue releases the accumulator on the even CTA's
+//    barrier.
+//  * 3xTF32: each producer also loads the lo part of its operand (written by
+//    the split pre-pass) into the stage; the MMA thread issues three MMAs per
+//    k-step.
 //  * Before leaving, each CTA waits (bounded) for every signal still heading
 //    its way, then both CTAs meet at a cluster barrier and free TMEM.
 template <TcKind KIND, bool AT_ = false, bool BT_ = false>
