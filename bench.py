@@ -336,6 +336,29 @@ def cpu_oracle_rate(seconds, chunk=8):
     return flops / el / 1e12, done, threads, el
 
 
+def cpu_oracle_small():
+    """Seconds the oracle (C only) takes on the three small workloads, on one
+    host thread and on all of them."""
+    import oracle
+    from dense_gemm_f32_gb300 import inputs
+
+    out, nmax = {}, oracle.max_threads()
+    try:
+        for w in (inputs.SQUARE_64, inputs.SQUARE_1024, inputs.RAGGED_1000):
+            A, B = inputs.make(w)
+            An, Bn = A.float().numpy(), B.float().numpy()
+            row = {}
+            for n in (1, nmax):
+                oracle.set_threads(n)
+                t0 = time.perf_counter()
+                oracle.gemm(An, Bn)
+                row[f"s_{n}_thread{'s' if n > 1 else ''}"] = round(time.perf_counter() - t0, 4)
+            out[w.name] = row
+    finally:
+        oracle.set_threads(nmax)
+    return out
+
+
 def run_reference(args, dist):
     """--impl reference: the CPU oracle timed as the reference arm."""
     if dist.rank != 0:
@@ -714,7 +737,8 @@ def run_ours(args, dist):
         v, rows, threads, secs = cpu_oracle_rate(args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"first {rows} full rows of C of the {inputs_name()} workload "
-                         f"({secs:.1f} s, FP64 accumulation, OpenMP over rows)"}
+                         f"({secs:.1f} s, FP64 accumulation, OpenMP over rows)",
+               "small_workloads": cpu_oracle_small()}
 
     if dist.rank == 0:
         line = {
