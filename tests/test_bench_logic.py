@@ -126,3 +126,16 @@ def test_reference_line_shape(capsys):
     for k in ("impl", "metric", "value", "unit", "cpu_baseline", "e2e", "config"):
         assert k in line
     assert line["impl"] == "reference" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_oracle_small_workloads_times_both_thread_counts():
+    """The small-workload oracle timings of cpu_baseline: one entry per small
+    workload, one and all host threads, and the thread count restored."""
+    import oracle
+
+    n = oracle.max_threads()
+    out = bench.cpu_oracle_small()
+    assert set(out) == {"square-64 fp32", "square-1024 fp32", "ragged 1000x1013x997 fp32"}
+    for row in out.values():
+        assert len(row) == (2 if n > 1 else 1) and all(v >= 0 for v in row.values())
+    assert oracle.max_threads() == n
