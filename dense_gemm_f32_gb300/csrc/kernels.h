@@ -97,6 +97,11 @@ cudaError_t scratch_free(void *ptr, cudaStream_t stream);
 // Count one successful kernel launch (dgemm_kernel_launches).
 void count_launch();
 
+// Device address of the current device's watchdog word (0, or the site code
+// of the first bounded wait that gave up in any kernel of the library);
+// nullptr if it cannot be looked up.
+int *watchdog_address();
+
 // Read and clear the device's watchdog word after synchronising `stream`.
 cudaError_t read_watchdog(cudaStream_t stream, int *code);
 

@@ -5,24 +5,29 @@
 // buffering, a register tile per thread) with the structure of
 // "第八课：GPU 如何完成矩阵乘法": C_tile = sum_t A_tile,t x B_tile,t (section 九),
 // accumulation in registers with one store per element (section 十四),
-// multi-level block / warp / thread tiling (section 十九), double-buffered
-// shared memory (section 二十四), zero-fill and masked stores at the edges
-// (section 二十六), padding against bank conflicts (section 二十七).
+// multi-level block / warp / thread tiling (section 十九), copies that run
+// ahead of the arithmetic (sections 二十三-二十五), zero-fill and masked
+// stores at the edges (section 二十六), no bank conflicts (section 二十七).
 //
-// Shipped shape (chosen by measurement on GB300 over tile shapes, BK, lane
-// orders, unroll depths and packed fma.rn.f32x2 variants): block tile
-// 128 x 256 x 16, 256 threads as 2 x 4 warps of 64 x 64, lanes 8 x 4, an
-// 8 x 16 register tile per thread, one CTA per SM, the inner product in
-// packed two-wide FMAs (DGEMM_SIMT_FFMA2).
-// GB300 specifics that differ from the pages' kernels:
-//  * A is stored transposed (k-major) in shared memory so that both operand
-//    fragments are read with 128-bit shared loads; its rows carry a 4-float
-//    pad that keeps the transposed stores free of bank conflicts.
-//  * Every 128-bit fragment load of a warp reads one contiguous line.
-//  * Global loads are 128-bit where the operand rows are 16-byte aligned
-//    (template kVec); ragged edges fall back to masked scalar loads.
-//  * Thread blocks walk the C tiles in groups of 8 tile rows so that panels
-//    of A and B are re-read from L2 instead of HBM.
+// Two kernels:
+//  * sgemm_ring_kernel (operands TMA can address, B stored K x N): the
+//    global -> shared copies are TMA boxes into a ring of STAGES stages,
+//    each with a "full" mbarrier (the copy's bytes landed) and an "empty"
+//    mbarrier (every warp is done reading it).  No thread stages data in
+//    registers and there is no block-wide barrier in the main loop; the lane
+//    that refills a stage rotates over the warps.  A lands k-contiguous in
+//    128B-swizzled rows (or k-major when stored K x M) and every thread owns
+//    rows 8 apart, so one 128-bit shared load per row gives four k values
+//    and the eight rows of a warp's load fall in eight different bank groups.
+//  * sgemm_simt_kernel (other operands: rows that are not 16-byte aligned, B
+//    stored N x K, and small problems): 128-bit global loads into registers,
+//    stored to one of two shared buffers (A transposed, +4-float row pad),
+//    one block-wide barrier per k-block.
+// Both issue the inner product as packed fma.rn.f32x2: each row of the
+// register tile does {a_i, a_i} x {b_2h, b_2h+1} + acc, every multiply-add
+// rounded once in k order, so C is bitwise what scalar FFMAs give.
+// Shapes were chosen by measurement on GB300 (tile shapes, stages, warp and
+// lane layouts, FMA order).
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -34,6 +39,7 @@
 #include "kernels.h"
 #include "launch.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 // This file is compiled once per operand layout: DGEMM_SIMT_UNIT = 2 * AT + BT
 // (AT: A stored K x M; BT: B stored N x K), so the layouts compile in
@@ -79,6 +85,158 @@ __device__ __forceinline__ float4 load4(const float *__restrict__ X, int64_t ld,
     }
   }
   return v;
+}
+
+// After a kernel's main loop: the thread's TM x TN accumulators, acc[i][4h ..
+// 4h + 3] at tile row row_of(i) and tile columns col_of(h) .. + 3, go to C.
+//  * Whole tile: masked stores, 128-bit where C's rows are 16-byte aligned.
+//  * K-split over a cluster (every tile split, cluster_parts != 0): the part
+//    parks its partial tile in its own shared memory at `park` (BM rows of
+//    PART_PITCH floats; the caller has made sure nothing else uses it any
+//    more), then each CTA adds one slice of the tile's rows over all parts,
+//    in part order, through distributed shared memory and writes it to C.
+//    Every thread reaches both cluster barriers.
+//  * K-split through scratch (the tiles of a partial last wave): the part
+//    writes its partial tile to `work`; the last part to finish (an atomic
+//    counter) sums all parts in part order, so the result does not depend on
+//    which finishes last, and writes C.
+template <int BM, int BN, int THREADS, int TM, int TN, int PART_PITCH, class RowOf, class ColOf>
+__device__ __forceinline__ void finish_tile(const float (&acc)[TM][TN], RowOf row_of, ColOf col_of,
+                                            float *park, int M, int N, float *__restrict__ C,
+                                            int64_t ldc, int c_vec, int m0, int n0, bool split,
+                                            int tile, int part, int split_first, int split_parts,
+                                            float *__restrict__ work,
+                                            unsigned int *__restrict__ counters,
+                                            int cluster_parts) {
+  const int tid = threadIdx.x;
+  if (split && cluster_parts) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int rl = row_of(i);
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h)
+        *reinterpret_cast<float4 *>(park + rl * PART_PITCH + col_of(h)) =
+            make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
+    }
+    __syncwarp();
+    cluster_sync();  // partials written (release) and visible (acquire)
+    const int rank = (int)cluster_ctarank();
+    const int r0 = (BM * rank) / split_parts, r1 = (BM * (rank + 1)) / split_parts;
+    constexpr int Q = BN / 4;
+    const uint32_t base = smem_u32(park);
+    uint32_t peer[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) peer[p] = p < split_parts ? mapa_shared(base, (uint32_t)p) : 0u;
+    for (int e = tid; e < (r1 - r0) * Q; e += THREADS) {
+      const int rl = r0 + e / Q, cl = 4 * (e % Q);
+      const uint32_t off = (uint32_t)((rl * PART_PITCH + cl) * 4);
+      float4 v[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+        if (p < split_parts) v[p] = ld_cluster_f4(peer[p] + off);
+      float4 sum = v[0];  // parts added in K order
+#pragma unroll
+      for (int p = 1; p < 8; ++p)
+        if (p < split_parts) sum.x += v[p].x, sum.y += v[p].y, sum.z += v[p].z, sum.w += v[p].w;
+      const int r = m0 + rl, c = n0 + cl;
+      if (r < M) {
+        float *d = C + (int64_t)r * ldc + c;
+        if (c_vec && c + 3 < N) {
+          *reinterpret_cast<float4 *>(d) = sum;
+        } else {
+          if (c < N) d[0] = sum.x;
+          if (c + 1 < N) d[1] = sum.y;
+          if (c + 2 < N) d[2] = sum.z;
+          if (c + 3 < N) d[3] = sum.w;
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while a peer may still read its partial
+    return;
+  }
+
+  if (split) {
+    const int64_t slot = (int64_t)(tile - split_first) * split_parts;
+    float *mine = work + (slot + part) * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int rl = row_of(i);
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h)
+        *reinterpret_cast<float4 *>(mine + rl * BN + col_of(h)) =
+            make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int last;
+    if (threadIdx.x == 0)
+      last = atomicAdd(&counters[tile - split_first], 1u) == (unsigned)(split_parts - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // Sum the parts in part order and write C.  The accumulators are dead
+    // here, so the tile is walked as a flat array of float4s (consecutive
+    // threads, consecutive columns): a batch of CH float4s per thread is
+    // loaded from one part at a time, all in flight together, so each part
+    // costs one L2 round trip per batch.  -0 + x is x exactly, so the first
+    // add copies part 0.
+    const float *parts0 = work + slot * (BM * BN);
+    constexpr int Q = BN / 4;                      // float4s per tile row
+    constexpr int V = BM * Q / THREADS;            // float4s per thread
+    constexpr int CH = V < 16 ? V : 16;
+    static_assert(V % CH == 0, "whole batches");
+#pragma unroll 1
+    for (int c0 = 0; c0 < V; c0 += CH) {
+      float4 sum[CH];
+#pragma unroll
+      for (int q = 0; q < CH; ++q) sum[q] = make_float4(-0.f, -0.f, -0.f, -0.f);
+      for (int p = 0; p < split_parts; ++p) {
+        const float4 *src = reinterpret_cast<const float4 *>(parts0 + (int64_t)p * (BM * BN));
+#pragma unroll
+        for (int q = 0; q < CH; ++q) {
+          const float4 v = __ldcg(src + (c0 + q) * THREADS + tid);
+          sum[q].x += v.x, sum[q].y += v.y, sum[q].z += v.z, sum[q].w += v.w;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < CH; ++q) {
+        const int e = (c0 + q) * THREADS + tid;
+        const int r = m0 + e / Q, c = n0 + (e % Q) * 4;
+        if (r >= M) continue;
+        float *d = C + (int64_t)r * ldc + c;
+        if (c_vec && c + 3 < N) {
+          *reinterpret_cast<float4 *>(d) = sum[q];
+        } else {
+          if (c < N) d[0] = sum[q].x;
+          if (c + 1 < N) d[1] = sum[q].y;
+          if (c + 2 < N) d[2] = sum[q].z;
+          if (c + 3 < N) d[3] = sum[q].w;
+        }
+      }
+    }
+    if (threadIdx.x == 0) counters[tile - split_first] = 0u;
+    return;
+  }
+
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int r = m0 + row_of(i);
+    if (r >= M) continue;
+    float *crow = C + (int64_t)r * ldc;
+#pragma unroll
+    for (int h = 0; h < TN / 4; ++h) {
+      const int c = n0 + col_of(h);
+      const float *w = &acc[i][h * 4];
+      if (c_vec && c + 3 < N) {
+        *reinterpret_cast<float4 *>(crow + c) = make_float4(w[0], w[1], w[2], w[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (c + j < N) crow[c + j] = w[j];
+      }
+    }
+  }
 }
 
 // Block tile BM x BN x BK, WM x WN warps, each warp a (BM/WM) x (BN/WN) tile
@@ -283,148 +441,255 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
     for (int h = 0; h < TN / 2; ++h)
       asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[i][2 * h]), "=f"(acc[i][2 * h + 1]) : "l"(acc2[i][h]));
 #endif
+  finish_tile<BM, BN, G::THREADS, TM, TN, G::PART_PITCH>(
+      acc, [&](int i) { return row_base + (i / 4) * G::LM * 4 + (i % 4); },
+      [&](int h) { return col_base + h * G::LN * 4; }, reinterpret_cast<float *>(simt_smem), M, N,
+      C, ldc, c_vec, m0, n0, split, tile, part, split_first, split_parts, work, counters,
+      cluster_parts);
+}
 
-  if (split && cluster_parts) {
-    // Every tile is split and the parts of a tile form one thread-block
-    // cluster (CTA rank = part): park the partial tile in this CTA's shared
-    // memory (free since the main loop's last barrier), then each CTA adds
-    // one slice of the tile's rows over all parts, in part order, through
-    // distributed shared memory and writes it to C.  Every thread reaches
-    // both cluster barriers.
-    float *park = reinterpret_cast<float *>(simt_smem);
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-      const int rl = row_base + (i / 4) * G::LM * 4 + (i % 4);
-#pragma unroll
-      for (int h = 0; h < TN / 4; ++h)
-        *reinterpret_cast<float4 *>(park + rl * G::PART_PITCH + col_base + h * G::LN * 4) =
-            make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
-    }
-    __syncwarp();
-    cluster_sync();  // partials written (release) and visible (acquire)
-    const int rank = (int)cluster_ctarank();
-    const int r0 = (BM * rank) / split_parts, r1 = (BM * (rank + 1)) / split_parts;
-    constexpr int Q = BN / 4;
-    const uint32_t base = smem_u32(park);
-    uint32_t peer[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) peer[p] = p < split_parts ? mapa_shared(base, (uint32_t)p) : 0u;
-    for (int e = tid; e < (r1 - r0) * Q; e += G::THREADS) {
-      const int rl = r0 + e / Q, cl = 4 * (e % Q);
-      const uint32_t off = (uint32_t)((rl * G::PART_PITCH + cl) * 4);
-      float4 v[8];
-#pragma unroll
-      for (int p = 0; p < 8; ++p)
-        if (p < split_parts) v[p] = ld_cluster_f4(peer[p] + off);
-      float4 sum = v[0];  // parts added in K order
-#pragma unroll
-      for (int p = 1; p < 8; ++p)
-        if (p < split_parts) sum.x += v[p].x, sum.y += v[p].y, sum.z += v[p].z, sum.w += v[p].w;
-      const int r = m0 + rl, c = n0 + cl;
-      if (r < M) {
-        float *d = C + (int64_t)r * ldc + c;
-        if (c_vec && c + 3 < N) {
-          *reinterpret_cast<float4 *>(d) = sum;
-        } else {
-          if (c < N) d[0] = sum.x;
-          if (c + 1 < N) d[1] = sum.y;
-          if (c + 2 < N) d[2] = sum.z;
-          if (c + 3 < N) d[3] = sum.w;
-        }
-      }
-    }
-    __syncwarp();
-    cluster_sync();  // no CTA leaves while a peer may still read its partial
-    return;
-  }
+// ---------------------------------------------------------------------------
+// TMA ring kernel.  Block tile BM x BN, k-block BK = 32 (one 128-byte row of
+// A), WM x WN warps of 64 x (4 * TN) outputs, lanes 8 (lm) x 4 (ln), an
+// 8 x TN register tile per thread:
+//  * row i (i < 8) of a thread is tile row wm * 64 + lm + 8 i for A stored
+//    M x K (A's shared tile [m][k] in 128B-swizzled rows: 16-byte chunk q of
+//    row r sits at chunk q ^ (r & 7), so the eight rows lm + 8 i of a warp's
+//    load are in eight different bank groups), or wm * 64 + 4 lm + 32 (i / 4)
+//    + i % 4 for A stored K x M (shared tile [k][m], four consecutive rows
+//    per 128-bit load);
+//  * column block h (h < TN / 4) is tile columns wn * 4 TN + 4 ln + 16 h ..
+//    + 3 of B's shared tile [k][n].
+template <int BM_, int BN_, int WM_, int WN_, int TN_, int STAGES_, int MIN_BLOCKS_>
+struct RingCfg {
+  static constexpr int BM = BM_, BN = BN_, BK = 32, WM = WM_, WN = WN_;
+  static constexpr int LM = 8, LN = 4, TM = 8, TN = TN_;
+  static constexpr int THREADS = WM * WN * 32, NWARPS = WM * WN;
+  static constexpr int WTM = LM * TM, WTN = LN * TN;  // warp tile
+  static_assert(WM * WTM == BM && WN * WTN == BN, "the warps tile the block");
+  static_assert(TN % 4 == 0, "column blocks of 4");
+  static constexpr int STAGES = STAGES_, MIN_BLOCKS = MIN_BLOCKS_;
+  // A stage is refilled by the warp that finishes k-block i + 1 of the CTA's
+  // range, once every warp is done with k-block i (the stage's next load is
+  // then STAGES - 2 k-blocks ahead of the fastest warp).
+  static constexpr int LAG = 2;
+  static_assert(STAGES >= 3, "at least one k-block of look-ahead");
+  static constexpr int A_BYTES = BM * BK * 4, B_BYTES = BK * BN * 4;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static_assert(A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  // Cluster K-split: the part's partial tile parked over the idle ring.
+  static constexpr int PART_PITCH = BN + 4;
+  static constexpr int PART_BYTES = BM * PART_PITCH * 4;
+  static constexpr int DATA_BYTES = RING_BYTES > PART_BYTES ? RING_BYTES : PART_BYTES;
+  // full and empty barriers, the count of issued k-blocks, the abort flag
+  static constexpr int TAIL_BYTES = 2 * STAGES * 8 + 8;
+  static constexpr int SMEM_BYTES = 1024 + DATA_BYTES + TAIL_BYTES;  // 1024: alignment slack
+};
 
+// Watchdog site codes of the ring kernel (role * 16 + place).
+enum : int {
+  kSiteRingFull = 0x51,   // a warp's wait for a stage's copy
+  kSiteRingEmpty = 0x52,  // a refill's wait for the warps to release a stage
+  kSiteRingDrain = 0x53,  // the wait for copies still in flight after an abort
+};
+
+template <class G, bool AT>
+__global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
+    sgemm_ring_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, int M, int N, int K,
+                      float *__restrict__ C, int64_t ldc, int c_vec, int split_first,
+                      int split_parts, float *__restrict__ work,
+                      unsigned int *__restrict__ counters, int cluster_parts, int *watchdog) {
+  constexpr int BM = G::BM, BN = G::BN, BK = G::BK, TM = G::TM, TN = G::TN, S = G::STAGES;
+  pdl_launch_dependents();
+  extern __shared__ uint8_t ring_smem_raw[];
+  const uint32_t raw = smem_u32(ring_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128B swizzle atoms: 1024-byte aligned
+  uint8_t *smem = ring_smem_raw + (base - raw);
+  const uint32_t bars = base + G::DATA_BYTES;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  int *issued = reinterpret_cast<int *>(smem + G::DATA_BYTES + 16 * S);
+  volatile int *abort_flag = issued + 1;
+
+  // ---- work unit -> (tile, K range), as in sgemm_simt_kernel
+  const int KT = (K + BK - 1) / BK;
+  const bool split = split_parts > 1 && (int)blockIdx.x >= split_first;
+  int tile = blockIdx.x, part = 0, kt_begin = 0, kt_end = KT;
   if (split) {
-    // Park this part's partial tile; the last part to finish sums all parts
-    // in part order (so the result does not depend on which finishes last)
-    // and writes C.
-    const int64_t slot = (int64_t)(tile - split_first) * split_parts;
-    float *mine = work + (slot + part) * (BM * BN);
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-      const int rl = row_base + (i / 4) * G::LM * 4 + (i % 4);
-#pragma unroll
-      for (int h = 0; h < TN / 4; ++h) {
-        const int cl = col_base + h * G::LN * 4;
-        *reinterpret_cast<float4 *>(mine + rl * BN + cl) =
-            make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
-      }
-    }
-    __threadfence();
-    __syncthreads();
-    __shared__ int last;
-    if (threadIdx.x == 0)
-      last = atomicAdd(&counters[tile - split_first], 1u) == (unsigned)(split_parts - 1);
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    // Sum the parts in part order and write C.  The accumulators are dead
-    // here, so the tile is walked as a flat array of float4s (consecutive
-    // threads, consecutive columns): a batch of CH float4s per thread is
-    // loaded from one part at a time, all in flight together, so each part
-    // costs one L2 round trip per batch.  -0 + x is x exactly, so the first
-    // add copies part 0.
-    const float *parts0 = work + slot * (BM * BN);
-    constexpr int Q = BN / 4;                         // float4s per tile row
-    constexpr int V = BM * Q / G::THREADS;            // float4s per thread
-    constexpr int CH = V < 16 ? V : 16;
-    static_assert(V % CH == 0, "whole batches");
-#pragma unroll 1
-    for (int c0 = 0; c0 < V; c0 += CH) {
-      float4 sum[CH];
-#pragma unroll
-      for (int q = 0; q < CH; ++q) sum[q] = make_float4(-0.f, -0.f, -0.f, -0.f);
-      for (int p = 0; p < split_parts; ++p) {
-        const float4 *src = reinterpret_cast<const float4 *>(parts0 + (int64_t)p * (BM * BN));
-#pragma unroll
-        for (int q = 0; q < CH; ++q) {
-          const float4 v = __ldcg(src + (c0 + q) * G::THREADS + tid);
-          sum[q].x += v.x, sum[q].y += v.y, sum[q].z += v.z, sum[q].w += v.w;
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < CH; ++q) {
-        const int e = (c0 + q) * G::THREADS + tid;
-        const int r = m0 + e / Q, c = n0 + (e % Q) * 4;
-        if (r >= M) continue;
-        float *d = C + (int64_t)r * ldc + c;
-        if (c_vec && c + 3 < N) {
-          *reinterpret_cast<float4 *>(d) = sum[q];
-        } else {
-          if (c < N) d[0] = sum[q].x;
-          if (c + 1 < N) d[1] = sum[q].y;
-          if (c + 2 < N) d[2] = sum[q].z;
-          if (c + 3 < N) d[3] = sum[q].w;
-        }
-      }
-    }
-    if (threadIdx.x == 0) counters[tile - split_first] = 0u;
-    return;
+    const int u = blockIdx.x - split_first;
+    tile = split_first + u / split_parts;
+    part = u % split_parts;
+    const int per = (KT + split_parts - 1) / split_parts;
+    kt_begin = min(KT, part * per);
+    kt_end = min(KT, kt_begin + per);
   }
+  const int nkb = kt_end - kt_begin;
+  const int tiles_m = (M + BM - 1) / BM;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int per_group = kGroupM * tiles_n;
+  const int group = tile / per_group;
+  const int first_m = group * kGroupM;
+  const int gsize = min(tiles_m - first_m, kGroupM);
+  const int in_group = tile - group * per_group;
+  const int m0 = (first_m + in_group % gsize) * BM;
+  const int n0 = (in_group / gsize) * BN;
 
-  // ---- epilogue: masked stores, 128-bit where C rows are 16-byte aligned
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), G::NWARPS);
+    }
+    *issued = 0;
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  __syncthreads();
+  pdl_wait();  // set-up done; the previous kernel on the stream has completed
+
+  // k-block i of this CTA's range -> stage i % S.  The copy's bytes are
+  // announced before it is issued; boxes reaching past M, N or K are
+  // zero-filled and still count in full.
+  auto issue = [&](int i) {
+    const int s = i % S;
+    const int k0 = (kt_begin + i) * BK;
+    const uint32_t dst = base + (uint32_t)(s * G::STAGE_BYTES);
+    mbar_arrive_expect_tx(full_bar(s), (uint32_t)G::STAGE_BYTES);
+    if constexpr (AT)
+      tma_load_2d(dst, &tmap_a, full_bar(s), m0, k0);
+    else
+      tma_load_2d(dst, &tmap_a, full_bar(s), k0, m0);
+    tma_load_2d(dst + G::A_BYTES, &tmap_b, full_bar(s), n0, k0);
+    atomicAdd(issued, 1);
+  };
+  if (tid == 0)
+    for (int i = 0; i < nkb && i < S; ++i) issue(i);
+
+  const int wm = warp / G::WN, wn = warp % G::WN;
+  const int lm = lane >> 2, ln = lane & 3;
+  auto row_of = [&](int i) {
+    return AT ? wm * G::WTM + lm * 4 + (i >> 2) * 32 + (i & 3) : wm * G::WTM + lm + 8 * i;
+  };
+  auto col_of = [&](int h) { return wn * G::WTN + ln * 4 + 16 * h; };
+  // byte offsets within a stage
+  const uint32_t a_thr = AT ? (uint32_t)((wm * G::WTM + lm * 4) * 4)
+                            : (uint32_t)((wm * G::WTM + lm) * (BK * 4));
+  const uint32_t b_thr = (uint32_t)(G::A_BYTES + (wn * G::WTN + ln * 4) * 4);
+  auto lds4 = [&](uint32_t off) { return *reinterpret_cast<const float4 *>(smem + off); };
+
+  uint64_t acc2[TM][TN / 2];
 #pragma unroll
-  for (int i = 0; i < TM; ++i) {
-    const int r = m0 + row_base + (i / 4) * G::LM * 4 + (i % 4);
-    if (r >= M) continue;
-    float *crow = C + (int64_t)r * ldc;
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int h = 0; h < TN / 2; ++h) acc2[i][h] = 0ull;  // two +0.0f
+
+  // acc[i][2h .. 2h+1] += {a_i, a_i} x {b_2h, b_2h+1}: all a_i duplicated
+  // first, then the products column pair by column pair.
+  auto fma_block = [&](const float (&a)[TM], const float4 (&b4)[TN / 4]) {
+    uint64_t aa[TM], bb[TN / 2];
+#pragma unroll
+    for (int i = 0; i < TM; ++i) asm("mov.b64 %0, {%1, %1};" : "=l"(aa[i]) : "f"(a[i]));
 #pragma unroll
     for (int h = 0; h < TN / 4; ++h) {
-      const int c = n0 + col_base + h * G::LN * 4;
-      const float *w = &acc[i][h * 4];
-      if (c_vec && c + 3 < N) {
-        *reinterpret_cast<float4 *>(crow + c) = make_float4(w[0], w[1], w[2], w[3]);
-      } else {
+      asm("mov.b64 %0, {%1, %2};" : "=l"(bb[2 * h]) : "f"(b4[h].x), "f"(b4[h].y));
+      asm("mov.b64 %0, {%1, %2};" : "=l"(bb[2 * h + 1]) : "f"(b4[h].z), "f"(b4[h].w));
+    }
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (c + j < N) crow[c + j] = w[j];
+    for (int h = 0; h < TN / 2; ++h)
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i][h]) : "l"(aa[i]), "l"(bb[h]));
+  };
+  auto comp = [](const float4 &v, int t) { return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w; };
+
+  for (int it = 0; it < nkb; ++it) {
+    const int s = it % S;
+    const uint32_t ph = (uint32_t)(it / S) & 1u;
+    bool got = mbar_try_wait(full_bar(s), ph) || (!*abort_flag && mbar_wait(full_bar(s), ph));
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0 && !*abort_flag) {
+        atomicCAS(watchdog, 0, kSiteRingFull);
+        *abort_flag = 1;
+      }
+      break;
+    }
+    const uint32_t st = (uint32_t)(s * G::STAGE_BYTES);
+    if constexpr (!AT) {
+#pragma unroll
+      for (int q = 0; q < BK / 4; ++q) {
+        float4 a4[TM];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+          a4[i] = lds4(st + a_thr + i * 8 * (BK * 4) + (((uint32_t)q ^ (uint32_t)lm) << 4));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          float4 b4[TN / 4];
+#pragma unroll
+          for (int h = 0; h < TN / 4; ++h) b4[h] = lds4(st + b_thr + (4 * q + t) * (BN * 4) + 64 * h);
+          float a[TM];
+#pragma unroll
+          for (int i = 0; i < TM; ++i) a[i] = comp(a4[i], t);
+          fma_block(a, b4);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < BK; ++kk) {
+        float4 a4[TM / 4], b4[TN / 4];
+#pragma unroll
+        for (int c = 0; c < TM / 4; ++c) a4[c] = lds4(st + a_thr + kk * (BM * 4) + c * 128);
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h) b4[h] = lds4(st + b_thr + kk * (BN * 4) + 64 * h);
+        float a[TM];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) a[i] = comp(a4[i >> 2], i & 3);
+        fma_block(a, b4);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(s));
+    // Refill: the stage of k-block it + 1 - LAG gets k-block it + 1 - LAG + S
+    // once every warp has released it; the refilling lane rotates.
+    if (lane == 0 && warp == it % G::NWARPS) {
+      const int done = it + 1 - G::LAG;
+      if (done >= 0 && done + S < nkb) {
+        const int ds = done % S;
+        const uint32_t dph = (uint32_t)(done / S) & 1u;
+        if (mbar_try_wait(empty_bar(ds), dph) || (!*abort_flag && mbar_wait(empty_bar(ds), dph))) {
+          issue(done + S);
+        } else if (!*abort_flag) {
+          atomicCAS(watchdog, 0, kSiteRingEmpty);
+          *abort_flag = 1;
+        }
       }
     }
   }
+  __syncthreads();
+  if (*abort_flag) {
+    // Only after an abort can copies still be in flight: at most the last S
+    // issued, one per stage.  Wait (bounded) for them, so that no TMA write
+    // lands after the CTA has left or while the ring is reused below.
+    if (tid == 0) {
+      const int n = *issued;
+      for (int i = n - 1; i >= 0 && i >= n - S; --i)
+        if (!mbar_wait(full_bar(i % S), (uint32_t)(i / S) & 1u)) atomicCAS(watchdog, 0, kSiteRingDrain);
+    }
+    __syncthreads();
+  }
+
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int h = 0; h < TN / 2; ++h)
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[i][2 * h]), "=f"(acc[i][2 * h + 1]) : "l"(acc2[i][h]));
+  finish_tile<BM, BN, G::THREADS, TM, TN, G::PART_PITCH>(
+      acc, row_of, col_of, reinterpret_cast<float *>(smem), M, N, C, ldc, c_vec, m0, n0, split,
+      tile, part, split_first, split_parts, work, counters, cluster_parts);
 }
 
 // Clusters of `size` CTAs of `kern` (threads, smem bytes each) that can be
@@ -460,6 +725,66 @@ int simt_active_clusters(const void *kern, int threads, int smem, int dev, int s
   return n;
 }
 
+// The grid of one SIMT launch of `kern` (threads per CTA, min_blocks CTAs
+// per SM, bm x bn tiles, KT k-blocks):
+//  * whole tiles, one CTA each;
+//  * when the tiles leave a last wave at most half full, that wave's tiles
+//    split along K into up to 8 parts of at least 4 k-blocks, one CTA each,
+//    partials through scratch (finish_tile);
+//  * when every tile is split (a small problem) and the parts' clusters are
+//    all resident at once, each tile's parts as one thread-block cluster,
+//    partials through distributed shared memory: no scratch, no second pass
+//    (a cluster that waits for a second wave doubles the time).
+// launch(grid, cluster, split_first, parts, work, counters, cluster_parts)
+// enqueues the kernel.
+template <class Launch>
+cudaError_t run_simt_grid(const void *kern, int threads, int smem_cluster, int min_blocks,
+                          int64_t tiles, int KT, int bm, int bn, int num_sms, cudaStream_t stream,
+                          Launch launch) {
+  const int64_t slots = (int64_t)num_sms * min_blocks;
+  const int64_t rem = slots > 0 ? tiles % slots : 0;
+  int parts = 1;
+  if (rem > 0) parts = (int)(slots / rem < 8 ? slots / rem : 8);
+  while (parts > 1 && KT < 4 * parts) --parts;  // keep at least 4 k-blocks per part
+  if (parts > 1 && rem == tiles) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (int p = parts; p >= 2; --p)
+      if (tiles <= simt_active_clusters(kern, threads, smem_cluster, dev, p))
+        return launch(tiles * p, p, (int64_t)0, p, static_cast<float *>(nullptr),
+                      static_cast<unsigned int *>(nullptr), 1);
+  }
+  if (parts <= 1)
+    return launch(tiles, 1, tiles, 1, static_cast<float *>(nullptr),
+                  static_cast<unsigned int *>(nullptr), 0);
+  const int64_t split_first = tiles - rem;
+  const int64_t grid = split_first + rem * parts;
+  const size_t work_bytes = (size_t)(rem * parts) * bm * bn * sizeof(float);
+  void *scratch = nullptr;
+  cudaError_t e = scratch_alloc(&scratch, work_bytes + (size_t)rem * sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return e;
+  float *work = static_cast<float *>(scratch);
+  unsigned int *counters =
+      reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + work_bytes);
+  e = cudaMemsetAsync(counters, 0, (size_t)rem * sizeof(unsigned int), stream);
+  if (e == cudaSuccess) e = launch(grid, 1, split_first, parts, work, counters, 0);
+  const cudaError_t e2 = scratch_free(scratch, stream);
+  return e == cudaSuccess ? e2 : e;
+}
+
+// Opt `kern` in to `smem` bytes of dynamic shared memory (once per device).
+template <class Kern>
+cudaError_t allow_smem(Kern kern, int smem, std::atomic<bool> (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 template <class G, bool AT, bool BT>
 cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, const float *B,
                             int64_t ldb, float *C, int64_t ldc, bool ab_vec, bool c_vec,
@@ -467,73 +792,55 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
   const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   auto kern = ab_vec ? sgemm_simt_kernel<G, true, AT, BT> : sgemm_simt_kernel<G, false, AT, BT>;
-  {
-    // opt in to the dynamic shared memory of the cluster K-split (per device, once)
-    static std::atomic<bool> done[2][64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !done[ab_vec][dev].load(std::memory_order_acquire)) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               G::SMEM_CLUSTER);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) done[ab_vec][dev].store(true, std::memory_order_release);
-    }
-  }
-  // Tail split: when the tiles leave a last wave that is at most half full,
-  // its tiles are split along K so that the wave's blocks finish sooner.
-  const int64_t slots = (int64_t)num_sms * G::MIN_BLOCKS;
-  const int64_t rem = tiles % slots;
+  static std::atomic<bool> done[2][64] = {};
+  cudaError_t e = allow_smem(kern, G::SMEM_CLUSTER, done[ab_vec]);
+  if (e != cudaSuccess) return e;
   const int KT = (K + G::BK - 1) / G::BK;
-  int parts = 1;
-  if (rem > 0 && num_sms > 0) parts = (int)(slots / rem < 8 ? slots / rem : 8);
-  while (parts > 1 && KT < 4 * parts) --parts;  // keep at least 4 k-blocks per part
-  int64_t split_first = tiles, grid = tiles;
-  float *work = nullptr;
-  unsigned int *counters = nullptr;
-  void *scratch = nullptr;
-  cudaError_t e = cudaSuccess;
-  int cparts = 0;  // cluster size for the all-split case, if its clusters fit at once
-  if (parts > 1 && rem == tiles) {
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    for (int p = parts; p >= 2 && cparts == 0; --p)
-      if (tiles <= simt_active_clusters(reinterpret_cast<const void *>(kern), G::THREADS,
-                                        G::SMEM_CLUSTER, dev, p))
-        cparts = p;
-  }
-  if (cparts > 1) {
-    // Every tile is split (a small problem): the parts of a tile run as one
-    // cluster and add their partials through distributed shared memory; no
-    // scratch, no second pass.  Only cluster sizes whose clusters are all
-    // resident at once are used: a cluster that waits for a second wave
-    // doubles the time.
-    parts = cparts;
-    return launch_kernel(kern, dim3((unsigned)(tiles * parts)), dim3(G::THREADS), G::SMEM_CLUSTER,
-                         stream, (unsigned)parts, M, N, K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0,
-                         0, parts, nullptr, nullptr, 1);
-  }
-  if (parts > 1) {
-    split_first = tiles - rem;
-    grid = split_first + rem * parts;
-    const size_t work_bytes = (size_t)(rem * parts) * G::BM * G::BN * sizeof(float);
-    e = scratch_alloc(&scratch, work_bytes + (size_t)rem * sizeof(unsigned int), stream);
-    if (e != cudaSuccess) return e;
-    work = static_cast<float *>(scratch);
-    counters = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + work_bytes);
-    e = cudaMemsetAsync(counters, 0, (size_t)rem * sizeof(unsigned int), stream);
-  }
-  if (e == cudaSuccess) {
-    e = launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream, 1, M, N,
-                      K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0, (int)split_first, parts, work,
-                      counters, 0);
-  }
-  if (scratch) {
-    const cudaError_t e2 = scratch_free(scratch, stream);
-    if (e == cudaSuccess) e = e2;
-  }
-  return e;
+  return run_simt_grid(
+      reinterpret_cast<const void *>(kern), G::THREADS, G::SMEM_CLUSTER, G::MIN_BLOCKS, tiles, KT,
+      G::BM, G::BN, num_sms, stream,
+      [&](int64_t grid, int cluster, int64_t split_first, int parts, float *work,
+          unsigned int *counters, int cparts) {
+        return launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS),
+                             cluster > 1 ? G::SMEM_CLUSTER : G::SMEM_BYTES, stream,
+                             (unsigned)cluster, M, N, K, A, lda, B, ldb, C, ldc, c_vec ? 1 : 0,
+                             (int)split_first, parts, work, counters, cparts);
+      });
+}
+
+// The TMA ring kernel for A stored M x K (AT = false) or K x M and B stored
+// K x N, both with 16-byte aligned rows.
+template <class G, bool AT>
+cudaError_t launch_ring_cfg(int M, int N, int K, const float *A, int64_t lda, const float *B,
+                            int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
+                            cudaStream_t stream) {
+  const int64_t tiles = (int64_t)((M + G::BM - 1) / G::BM) * ((N + G::BN - 1) / G::BN);
+  if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  const bool ok_a =
+      AT ? make_map(&ta, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, K, M, lda, G::BM, G::BK,
+                    CU_TENSOR_MAP_SWIZZLE_NONE)
+         : make_map(&ta, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, K, lda, G::BK, G::BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  const bool ok_b = make_map(&tb, B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, K, N, ldb, G::BN, G::BK,
+                             CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+  int *wd = watchdog_address();
+  if (wd == nullptr) return cudaErrorInvalidSymbol;
+  auto kern = sgemm_ring_kernel<G, AT>;
+  static std::atomic<bool> done[64] = {};
+  cudaError_t e = allow_smem(kern, G::SMEM_BYTES, done);
+  if (e != cudaSuccess) return e;
+  const int KT = (K + G::BK - 1) / G::BK;
+  return run_simt_grid(
+      reinterpret_cast<const void *>(kern), G::THREADS, G::SMEM_BYTES, G::MIN_BLOCKS, tiles, KT,
+      G::BM, G::BN, num_sms, stream,
+      [&](int64_t grid, int cluster, int64_t split_first, int parts, float *work,
+          unsigned int *counters, int cparts) {
+        return launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream,
+                             (unsigned)cluster, ta, tb, M, N, K, C, ldc, c_vec ? 1 : 0,
+                             (int)split_first, parts, work, counters, cparts, wd);
+      });
 }
 
 #if DGEMM_SIMT_UNIT == 0
@@ -551,7 +858,8 @@ __global__ void zero_fill_kernel(float *__restrict__ C, int M, int N, int64_t ld
 
 }  // namespace
 
-// The configuration the library ships (see the variant table in the design doc).
+// Register-staged kernel: 128 x 256 x 16 block tiles, 256 threads as 2 x 4
+// warps of 64 x 64, an 8 x 16 register tile per thread, one CTA per SM.
 // (DGEMM_SIMT_CFG overrides it for tuning sweeps: BM,BN,BK,WM,WN,LM,MIN_BLOCKS.)
 #ifndef DGEMM_SIMT_CFG
 #define DGEMM_SIMT_CFG 128, 256, 16, 2, 4, 8, 1
@@ -581,6 +889,21 @@ static bool simt_use_small(int M, int N, int num_sms) {
   return tm * tn * 8 < num_sms || padded >= 1.5 * (double)M * (double)N;
 }
 
+// TMA ring kernel: 128 x 256 tiles of 8 warps, one CTA per SM, 4 stages of
+// 48 KB (RingWide), or 128 x 128 tiles of 4 warps, two CTAs per SM, 3 stages
+// of 32 KB (RingSquare); 8 x 16 register tiles either way.
+using RingWide = RingCfg<128, 256, 2, 4, 16, 4, 1>;
+using RingSquare = RingCfg<128, 128, 2, 2, 16, 3, 2>;
+
+// Which kernel takes operands the ring kernel can read: 1 RingWide, 2
+// RingSquare, 0 the register-staged kernel.  DGEMM_SIMT_RING=0/1/2 forces
+// one (read on every call, for tests and tuning).
+static int simt_ring_choice() {
+  const char *e = getenv("DGEMM_SIMT_RING");
+  if (e && e[0] >= '0' && e[0] <= '2' && e[1] == 0) return e[0] - '0';
+  return 1;
+}
+
 // This unit's operand layout.
 cudaError_t DG_SIMT_UNIT_LAUNCHER(int M, int N, int K, const float *A, int64_t lda,
                                   const float *B, int64_t ldb, float *C, int64_t ldc, bool ab_vec,
@@ -588,6 +911,18 @@ cudaError_t DG_SIMT_UNIT_LAUNCHER(int M, int N, int K, const float *A, int64_t l
   if (simt_use_small(M, N, num_sms))
     return launch_simt_cfg<SimtSmall, kUnitAT, kUnitBT>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
                                                         c_vec, num_sms, stream);
+  if constexpr (!kUnitBT) {
+    // B stored K x N and both operands' rows 16-byte aligned: TMA can read them
+    if (ab_vec) {
+      const int ring = simt_ring_choice();
+      if (ring == 1)
+        return launch_ring_cfg<RingWide, kUnitAT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                                  stream);
+      if (ring == 2)
+        return launch_ring_cfg<RingSquare, kUnitAT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
+                                                    num_sms, stream);
+    }
+  }
   return launch_simt_cfg<SimtShipped, kUnitAT, kUnitBT>(M, N, K, A, lda, B, ldb, C, ldc, ab_vec,
                                                         c_vec, num_sms, stream);
 }

@@ -49,6 +49,7 @@
 #include "launch.cuh"
 #include "ptx.cuh"
 #include "tf32_split.cuh"
+#include "tmap.cuh"
 
 // This file is compiled once per operand layout: DGEMM_TC_UNIT = 2 * AT + BT
 // selects which kernels one translation unit instantiates (AT: A stored
@@ -1023,35 +1024,6 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
 }
 
 // ------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// 2-D row-major tensor map: `rows` x `cols` elements, leading dimension `ld`,
-// box of box_cols x box_rows, the given swizzle, zero fill out of range.
-bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es, int64_t rows,
-              int64_t cols, int64_t ld, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // Tile rows per raster group: `dflt` unless DGEMM_TC_GROUP_M (1..64)
 // overrides it for tuning sweeps; it changes only the order tiles are visited
 // in.  Measured best on GB300: 32 rows of 128-row tiles for the single-CTA
@@ -1345,7 +1317,6 @@ cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, in
 }
 
 #if DGEMM_TC_UNIT == 0
-namespace {
 // Device address of this device's watchdog word (looked up once per device).
 int *watchdog_address() {
   static std::atomic<int *> addr[64] = {};
@@ -1360,7 +1331,6 @@ int *watchdog_address() {
   }
   return a;
 }
-}  // namespace
 
 bool tc_use_pair(int M, int N, int num_sms) {
   const char *e = getenv("DGEMM_TC_PAIR");
