@@ -198,8 +198,17 @@ int gemm_bf16_tc(int M, int N, int K,
  *     they fit there; larger problems run on the single-CTA kernel, which
  *     needs no scratch for the split.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins on the device.
+ *     (cudaGetSymbolAddress) with that device current.  Under CUDA's lazy
+ *     module loading (the default) that lookup is also what loads the array
+ *     into device memory, so the first call on each device must come before
+ *     the caller reserves all device memory, and before any stream capture
+ *     begins on the device.  The address is kept for the life of the process:
+ *     do not use the library across cudaDeviceReset.
+ *   - Results are bitwise those of gemm_f32_tc in TF32 mode, and in 3xTF32
+ *     mode whenever the lo parts fit in the array (or the problem is small
+ *     enough for the single-CTA kernel anyway); larger 3xTF32 problems run
+ *     on a different kernel and agree with gemm_f32_tc only within the
+ *     3xTF32 tolerance.
  *   - Every call on a device shares the one array, and it keeps the last
  *     call's contents.  Each call overwrites all the scratch it reads before
  *     reading it, so nothing needs clearing; but two calls whose work

@@ -93,10 +93,13 @@ int main(void) {
         return fail("lda < K not rejected", st);
     if ((st = gemm_f32_tc(7, M, N, K, dA, K, dB, N, dC, N, 0)) != DGEMM_ERR_UNSUPPORTED)
         return fail("unknown mode not rejected", st);
+    if ((st = gemm_f32_tc_noalloc(7, M, N, K, dA, K, dB, N, dC, N, 0)) != DGEMM_ERR_UNSUPPORTED)
+        return fail("unknown no-alloc mode not rejected", st);
 
     struct { const char *name; int path; } paths[] = {
         {"simt", -1}, {"tf32", DGEMM_TC_TF32}, {"3xtf32", DGEMM_TC_3XTF32}, {"bf16", -2},
-        {"fp16", -3}, {"e4m3", -4}, {"gemm_ex 3xtf32 NT", -5}};
+        {"fp16", -3}, {"e4m3", -4}, {"gemm_ex 3xtf32 NT", -5}, {"tf32 no-alloc", -6},
+        {"3xtf32 no-alloc", -7}};
     int p;
     for (p = 0; p < (int)(sizeof paths / sizeof paths[0]); ++p) {
         cudaMemset(dC, 0xff, sizeof C);         /* NaN everywhere before the call */
@@ -129,6 +132,10 @@ int main(void) {
             case -5:
                 st = dgemm_gemm_ex(DGEMM_PATH_3XTF32, DGEMM_OP_N, DGEMM_OP_T, M, N, K, dA, K, dBt,
                                    K, dC, N, 0);
+                break;
+            case -6: st = gemm_f32_tc_noalloc(DGEMM_TC_TF32, M, N, K, dA, K, dB, N, dC, N, 0); break;
+            case -7:
+                st = gemm_f32_tc_noalloc(DGEMM_TC_3XTF32, M, N, K, dA, K, dB, N, dC, N, 0);
                 break;
             default: st = gemm_f32_tc(paths[p].path, M, N, K, dA, K, dB, N, dC, N, 0);
         }

@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
 P = 0x10000  # a fake, 16-byte aligned address: never dereferenced by these calls
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16", "noalloc-tf32", "noalloc-3xtf32"])
 def test_invalid_sizes_rejected(lib, fn):
     call = _caller(fn)
     E = dg.ERR_INVALID_VALUE
@@ -61,7 +61,7 @@ def test_invalid_sizes_rejected(lib, fn):
     assert call(4, 4, 0, P, 0, P * 2, 4, P * 3, 4) == E     # lda must be >= 1
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16", "noalloc-tf32", "noalloc-3xtf32"])
 def test_empty_output_is_a_no_op(lib, fn):
     call = _caller(fn)
     # nothing to do: pointers are not looked at, no CUDA call is made
@@ -69,7 +69,7 @@ def test_empty_output_is_a_no_op(lib, fn):
     assert call(5, 0, 5, 0, 5, 0, 1, 0, 1) == dg.OK
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16", "noalloc-tf32", "noalloc-3xtf32"])
 def test_null_pointers_rejected(lib, fn):
     call = _caller(fn)
     E = dg.ERR_NULL_POINTER
@@ -79,7 +79,7 @@ def test_null_pointers_rejected(lib, fn):
     assert call(4, 4, 0, P, 1, P * 2, 4, 0, 4) == E       # K == 0 still writes C
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16", "noalloc-tf32", "noalloc-3xtf32"])
 def test_misaligned_pointers_rejected(lib, fn):
     call = _caller(fn)
     es = 2 if fn in ("bf16", "fp16") else 4
@@ -91,7 +91,7 @@ def test_misaligned_pointers_rejected(lib, fn):
         assert call(4, 4, 4, P + 2, 4, P * 2, 4, P * 4, 4) == E
 
 
-@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16"])
+@pytest.mark.parametrize("fn", ["simt", "tf32", "3xtf32", "bf16", "fp16", "noalloc-tf32", "noalloc-3xtf32"])
 def test_alias_rejected(lib, fn):
     call = _caller(fn)
     es = 2 if fn in ("bf16", "fp16") else 4
@@ -103,9 +103,19 @@ def test_alias_rejected(lib, fn):
     assert call(8, 8, 8, P * 4 + 64, 8, P * 8, 8, P * 4, 8) == E
 
 
-def test_unknown_mode_rejected(lib):
-    assert dg.gemm_f32_tc(7, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
-    assert dg.gemm_f32_tc(-1, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+@pytest.mark.parametrize("fn", ["gemm_f32_tc", "gemm_f32_tc_noalloc"])
+def test_unknown_mode_rejected(lib, fn):
+    f = getattr(dg, fn)
+    assert f(7, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    assert f(-1, 4, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+    # the mode is checked before anything else, even with sizes that are invalid too
+    assert f(2, -1, 4, 4, P, 4, P * 2, 4, P * 4, 4, 0) == dg.ERR_UNSUPPORTED
+
+
+def test_scratch_limit_status_names_the_limit(lib):
+    s = dg.dgemm_status_string(dg.ERR_SCRATCH_LIMIT)
+    assert "16 MiB" in s and "gemm_f32_tc_noalloc" in s
+    assert dg.NOALLOC_SCRATCH_BYTES == 16 << 20
 
 
 def test_matmul_argument_checks_need_no_gpu():
@@ -134,6 +144,10 @@ def _caller(fn):
         return lambda *a: dg.gemm_f32_tc(dg.TC_3XTF32, *a, 0)
     if fn == "fp16":
         return lambda *a: dg.gemm_f16_tc(*a, 0)
+    if fn == "noalloc-tf32":
+        return lambda *a: dg.gemm_f32_tc_noalloc(dg.TC_TF32, *a, 0)
+    if fn == "noalloc-3xtf32":
+        return lambda *a: dg.gemm_f32_tc_noalloc(dg.TC_3XTF32, *a, 0)
     return lambda *a: dg.gemm_bf16_tc(*a, 0)
 
 

@@ -6,9 +6,10 @@ latency-critical loop that cannot afford an allocation failing mid-run.  For
 them the library keeps a fixed 16 MiB scratch array on each GPU and
 gemm_f32_tc_noalloc re-pitches unaligned operands into it instead of calling
 cudaMallocAsync.  These tests call it through the C ABI and check that it
-gives what gemm_f32_tc gives, within the tolerances the other tests use, on
-two calls in a row (the second with different inputs, so that a stale
-scratch would show), and that it refuses operands that do not fit.
+gives what gemm_f32_tc gives (bit for bit wherever both run the same kernel,
+within the tolerances the other tests use otherwise) and what the CPU oracle
+gives, on two calls in a row (the second with different inputs, so that a
+stale scratch would show), and that it refuses operands that do not fit.
 
 This file is collected last on purpose; it also passes when run on its own.
 """
@@ -58,6 +59,12 @@ def _s(A, B):
     return oracle.abs_gemm(A.float().cpu().numpy(), B.float().cpu().numpy())
 
 
+def _oracle(A, B):
+    import oracle
+
+    return oracle.gemm(A.float().cpu().numpy(), B.float().cpu().numpy())
+
+
 @pytest.mark.parametrize("mode", ["tf32", "3xtf32"])
 def test_matches_existing_entry_point_on_two_calls(mode):
     """Ragged shapes with rows that are not 16-byte aligned, so both operands
@@ -68,10 +75,9 @@ def test_matches_existing_entry_point_on_two_calls(mode):
         Ad, Bd = A.cuda(), B.cuda()
         ref, new = _pair(mode, Ad, Bd)
         assert np.isfinite(new).all()
-        S = _s(A, B)
-        err = np.abs(new.astype(np.float64) - ref.astype(np.float64))
-        assert np.all(err <= gu.TOL[mode] * S), f"{mode} {M}x{N}x{K}: max err/S " \
-            f"{float(np.max(err / np.where(S > 0, S, 1))):.3e}"
+        # the same kernel on the same operands: identical bits
+        assert np.array_equal(new, ref), f"{mode} {M}x{N}x{K}: differs from gemm_f32_tc"
+        gu.assert_close(new, _oracle(A, B), _s(A, B), gu.TOL[mode], f"{mode} {M}x{N}x{K}")
     gu.check_watchdog()
 
 
@@ -83,12 +89,12 @@ def test_only_b_misaligned_and_aligned_operands():
     Bd = gu.device_view(*inputs.embed(B, N, offset=1))
     assert Bd.data_ptr() % 16 != 0
     ref, new = _pair("tf32", Ad, Bd)
-    S = _s(A, B)
-    assert np.all(np.abs(new.astype(np.float64) - ref) <= gu.TOL["tf32"] * S)
+    assert np.array_equal(new, ref)
+    gu.assert_close(new, _oracle(A, B), _s(A, B), gu.TOL["tf32"], "only B re-pitched")
     A2, B2 = inputs.make_random(512, 512, 512, seed=9)
     ref, new = _pair("tf32", A2.cuda(), B2.cuda())
-    S = _s(A2, B2)
-    assert np.all(np.abs(new.astype(np.float64) - ref) <= gu.TOL["tf32"] * S)
+    assert np.array_equal(new, ref)
+    gu.assert_close(new, _oracle(A2, B2), _s(A2, B2), gu.TOL["tf32"], "aligned")
 
 
 def test_rejects_operands_beyond_the_scratch():
@@ -111,7 +117,10 @@ def test_3xtf32_lo_parts_in_the_fixed_scratch(K, launches):
     K = 512 the lo parts of A and B (8 MiB) fit in the fixed scratch, so the
     split pre-pass writes them there and the pair kernel loads them (two
     launches); with K = 2048 (32 MiB) they do not, and the single-CTA kernel
-    splits in shared memory (one launch).  Both match gemm_f32_tc."""
+    splits in shared memory (one launch).  With K = 512 both entry points run
+    the same kernel on the same operands and agree bit for bit; with K = 2048
+    gemm_f32_tc runs the pair kernel, which sums in another order, so the two
+    agree within the 3xTF32 tolerance.  Both match the oracle."""
     M = N = 2048
     A, B = inputs.make_random(M, N, K, seed=K, dist="normal")
     Ad, Bd = A.cuda(), B.cuda()
@@ -123,7 +132,10 @@ def test_3xtf32_lo_parts_in_the_fixed_scratch(K, launches):
     assert dg.dgemm_kernel_launches() - n0 == launches
     ref, new = _pair("3xtf32", Ad, Bd)
     S = _s(A, B)
+    if launches == 2:
+        assert np.array_equal(new, ref)
     err = np.abs(new.astype(np.float64) - ref.astype(np.float64))
     assert np.all(err <= gu.TOL["3xtf32"] * S)
     assert np.array_equal(C.cpu().numpy(), new)
+    gu.assert_close(new, _oracle(A, B), S, gu.TOL["3xtf32"], f"3xtf32 K={K}")
     gu.check_watchdog()
