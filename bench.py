@@ -105,37 +105,108 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def mode_peak(mode, peaks, num_sms):
-    """(bound, peak TFLOP/s, how) for a mode's kernel timed in a short loop."""
+def mode_peak(mode, peaks, num_sms, measured=None):
+    """(bound, peak TFLOP/s, how) for a mode's kernel timed in a short loop.
+
+    BF16 / FP16: the driver's measured cuBLAS BF16 burst.  TF32 (and 3xTF32,
+    whose MMA work is three TF32 products) and FP8: cuBLAS's own TF32 and FP8
+    rates measured in this run (`measured`, best of 10 at 8192^3), else the
+    BF16 burst scaled by the nominal dense-rate ratio.  SIMT: the FFMA peak,
+    SMs x 128 lanes x 2 flop x the maximum SM clock."""
+    measured = measured or {}
     if mode == "simt":
         mhz = peaks.get("sm_max_mhz", 2070.0)
         return "alu", num_sms * 128 * 2 * mhz * 1e6 / 1e12, (
             f"{num_sms} SMs x 128 FP32 lanes x 2 flop x {mhz:.0f} MHz")
     bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     if mode == "bf16":
-        return "tensor", bf16, "measured cuBLAS bf16 burst"
+        return "tensor", bf16, "measured cuBLAS bf16 burst (MEASURED_PEAKS)"
     if mode == "fp16":
-        return "tensor", bf16, "measured cuBLAS bf16 burst (fp16 and bf16 share the nominal rate)"
-    if mode in ("e4m3", "e5m2"):
-        r = NOMINAL_PF["fp8"] / NOMINAL_PF["bf16"]
-        return "tensor", bf16 * r, f"measured bf16 burst x nominal fp8/bf16 ratio {r:.1f}"
-    r = NOMINAL_PF["tf32"] / NOMINAL_PF["bf16"]
-    return "tensor", bf16 * r, f"measured bf16 burst x nominal tf32/bf16 ratio {r:.4f}"
+        return "tensor", bf16, ("measured cuBLAS bf16 burst (MEASURED_PEAKS; fp16 and bf16 share "
+                                "the nominal rate)")
+    key = "fp8" if mode in ("e4m3", "e5m2") else "tf32"
+    if measured.get(key):
+        what = ("torch._scaled_mm E4M3 8192^3" if key == "fp8" else
+                "torch.matmul fp32 8192^3 with TF32 allowed")
+        return "tensor", measured[key], f"measured in this run: cuBLAS {what}, best of 10"
+    return "tensor", nominal_peak(mode, peaks), (
+        f"fallback: measured bf16 burst x nominal {key}/bf16 ratio "
+        f"{NOMINAL_PF[key] / NOMINAL_PF['bf16']:.4f}")
+
+
+def nominal_peak(mode, peaks):
+    """The BF16 burst scaled by the nominal dense-rate ratio (a secondary
+    figure next to the measured TF32 / FP8 peaks)."""
+    bf16 = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    key = "fp8" if mode in ("e4m3", "e5m2") else "tf32" if mode in ("tf32", "3xtf32") else "bf16"
+    return bf16 * NOMINAL_PF[key] / NOMINAL_PF["bf16"]
+
+
+def measure_tensor_peaks(device, reps=10):
+    """cuBLAS's TF32 and FP8 (E4M3) rates at 8192^3 on this GPU, the best of
+    `reps` back-to-back calls after 3 warm-up calls: the roofline denominators
+    of the TF32 and FP8 modes.  A failed measurement is recorded, not raised."""
+    import torch
+
+    out, errors = {}, {}
+    n = 8192
+    flops = 2.0 * n ** 3
+    g = torch.Generator(device="cpu").manual_seed(12)
+    A = (2 * torch.rand(n, n, generator=g) - 1).to(device)
+    B = (2 * torch.rand(n, n, generator=g) - 1).to(device)
+
+    def best(fn):
+        # back to back, one event between consecutive calls (no host launch
+        # gap inside a timed interval), the fastest interval
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record()
+        for i in range(reps):
+            fn()
+            ev[i + 1].record()
+        torch.cuda.synchronize(device)
+        return flops / (min(ev[i].elapsed_time(ev[i + 1]) for i in range(reps)) * 1e-3) / 1e12
+
+    prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = True
+        C = torch.empty(n, n, device=device)
+        out["tf32"] = best(lambda: torch.matmul(A, B, out=C))
+    except Exception as e:  # noqa: BLE001 -- recorded in the line instead
+        errors["tf32"] = f"{type(e).__name__}: {e}"
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    try:
+        A8 = A.to(torch.float8_e4m3fn)
+        B8 = B.t().contiguous().t().to(torch.float8_e4m3fn)  # column-major, as cuBLAS wants
+        one = torch.tensor(1.0, device=device)
+        out["fp8"] = best(lambda: torch._scaled_mm(A8, B8, scale_a=one, scale_b=one,
+                                                   out_dtype=torch.float32))
+    except Exception as e:  # noqa: BLE001
+        errors["fp8"] = f"{type(e).__name__}: {e}"
+    if errors:
+        out["errors"] = errors
+    return out
 
 
 def kernel_name(mode, M, N, num_sms):
     """The kernel the library runs for this mode and shape: the CTA-pair
     tensor-core kernel once there are 256 x 256 tiles for at least a quarter
     of the SMs, else the single-CTA one (the library's own rule)."""
-    if mode == "simt":
-        return "sgemm_simt_kernel"
+    if mode == "simt":  # B stored K x N, 16-byte aligned rows: the TMA ring kernel
+        return "sgemm_ring_kernel (TMA ring)"
     pair_tiles = ((M + 255) // 256) * ((N + 255) // 256)
     return "tc2_gemm_kernel (CTA pair)" if pair_tiles * 4 >= num_sms else "tc_gemm_kernel"
 
 
 def source_sha(mode):
+    """Hash of the sources of a mode's kernel: a recorded traffic figure
+    applies only while it matches."""
     csrc = os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc")
-    files = ["simt.cu"] if mode == "simt" else ["tc.cu", "ptx.cuh", "tf32_split.cuh"]
+    files = (["simt.cu", "ptx.cuh", "tmap.cuh"] if mode == "simt"
+             else ["tc.cu", "ptx.cuh", "tf32_split.cuh", "tmap.cuh"])
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
@@ -143,24 +214,24 @@ def source_sha(mode):
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(mode, workload_name):
-    """DRAM bytes per launch from profiles/dram_traffic.md, or None when the
-    kernel's source has changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
-        return None
-    sha = source_sha(mode)
-    with open(path, encoding="utf-8") as f:
-        for ln in f:
-            cells = [c.strip() for c in ln.strip().strip("|").split("|")]
-            if len(cells) >= 4 and cells[0] == mode and cells[1] == workload_name:
-                if cells[2] != sha:
-                    return None
-                try:
-                    return float(cells[3])
-                except ValueError:
-                    return None
-    return None
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, from one ncu capture each (--clock-control none, one
+# launch), keyed by (mode, workload); `sha` is source_sha(mode) of the sources
+# the capture ran, so a figure goes stale (null in the line) as soon as the
+# kernel changes.  The summaries of these captures are in profiles/.
+RECORDED_TRAFFIC = {}
+
+
+def recorded_traffic(mode, workload_name, table=None):
+    """(bytes per launch, provenance) for a mode's kernel on a workload, or
+    (None, why) when nothing was recorded for the current sources."""
+    table = RECORDED_TRAFFIC if table is None else table
+    rec = table.get((mode, workload_name))
+    if rec is None:
+        return None, "no ncu capture recorded for this kernel and workload"
+    if rec["sha"] != source_sha(mode):
+        return None, f"stale: recorded for sources {rec['sha']}, now {source_sha(mode)}"
+    return float(rec["bytes"]), {k: v for k, v in rec.items() if k != "bytes"}
 
 
 class ClockSampler:
@@ -270,12 +341,16 @@ def summarize_clocks(rows, windows):
             "samples": len(inside), "note": note}
 
 
-def aggregate(local_ms, world, flops_per_rank, steps, all_max):
-    """Whole-job numbers from this rank's timed milliseconds: all ranks'
-    flops over the slowest rank's time (`all_max` reduces a float by max)."""
-    t_ms = all_max(local_ms)
-    total = world * flops_per_rank * steps
-    return {"ms_total": t_ms, "ms_per_step": t_ms / steps, "value": total / (t_ms * 1e-3) / 1e12}
+def aggregate(median_ms, total_ms, world, flops_per_rank, steps, all_max):
+    """Whole-job numbers from this rank's timed steps: all ranks' flops over
+    the slowest rank's median step (`value`, `ms_per_step`), and over the
+    slowest rank's bracketed total of the K steps (`value_from_total`).
+    `all_max` reduces a float by max over ranks."""
+    med = all_max(median_ms)
+    tot = all_max(total_ms)
+    return {"ms_per_step": med, "ms_total": tot,
+            "value": world * flops_per_rank / (med * 1e-3) / 1e12,
+            "value_from_total": world * flops_per_rank * steps / (tot * 1e-3) / 1e12}
 
 
 # ------------------------------------------------------------- distributed
@@ -467,28 +542,29 @@ def time_device(mode, Ad, Bd, C, steps, warmup, dist, device, ta=False, tb=False
 
 
 def cublas_same_run(mode, Ad, Bd, device, steps=10):
-    """cuBLAS (through torch) on the headline's operands, timed the same way:
-    a comparator for the roofline fraction, not part of the library.  None
-    for modes cuBLAS has no counterpart of (3xTF32) or when the call fails."""
+    """cuBLAS (through torch) on a mode's operands, timed the same way (median
+    of `steps` event-timed calls after 3 warm-up calls): a comparator for the
+    roofline fraction, not part of the library.  Returns (ms, None), or
+    (None, why) for a mode cuBLAS has no counterpart of (3xTF32) or a call
+    that fails."""
     import torch
 
+    if mode == "3xtf32":
+        return None, "no cuBLAS counterpart (split-precision TF32)"
+    prev = torch.backends.cuda.matmul.allow_tf32
     try:
         if mode in ("tf32", "simt"):
-            prev = torch.backends.cuda.matmul.allow_tf32
             torch.backends.cuda.matmul.allow_tf32 = mode == "tf32"
             fn = lambda: Ad @ Bd  # noqa: E731
-            restore = lambda: setattr(torch.backends.cuda.matmul, "allow_tf32", prev)  # noqa: E731
         elif mode in ("bf16", "fp16"):
             fn = lambda: torch.mm(Ad, Bd, out_dtype=torch.float32)  # noqa: E731
-            restore = lambda: None  # noqa: E731
         elif mode in ("e4m3", "e5m2"):
             Bt = Bd.t().contiguous().t()  # column-major B, as cuBLAS's FP8 kernels want
             one = torch.tensor(1.0, device=device)
             fn = lambda: torch._scaled_mm(Ad, Bt, scale_a=one, scale_b=one,  # noqa: E731
                                           out_dtype=torch.float32)
-            restore = lambda: None  # noqa: E731
         else:
-            return None
+            return None, f"unknown mode {mode}"
         for _ in range(3):
             fn()
         torch.cuda.synchronize(device)
@@ -498,10 +574,20 @@ def cublas_same_run(mode, Ad, Bd, device, steps=10):
             fn()
         ev[steps].record()
         torch.cuda.synchronize(device)
-        restore()
-        return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
-    except Exception:  # noqa: BLE001 -- a comparator must never fail the bench
-        return None
+        return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps)), None
+    except Exception as e:  # noqa: BLE001 -- a comparator must never fail the bench
+        return None, f"{type(e).__name__}: {e}"
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def cublas_entry(flops, ours_tflops, ms, why):
+    """The cuBLAS comparator's entry in the line: its rate and ours over it,
+    or why there is none."""
+    if ms is None:
+        return {"tflops": None, "why": why}
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"tflops": round(tf, 1), "frac_of_cublas": round(ours_tflops / tf, 4)}
 
 
 def time_graph(mode, Ad, Bd, C, device, calls=20, replays=7):
@@ -666,25 +752,34 @@ def run_ours(args, dist):
         remeasured = why or "another rank's window"
         r = time_device(mode, Ad, Bd, C, args.steps, args.warmup, dist, device, ta, tb, flush=flush)
     del flush
-    agg = aggregate(r["ms_total"], dist.world, w.flops, args.steps, lambda x: dist.max(x, device))
+    agg = aggregate(statistics.median(r["per_step_ms"]), r["ms_total"], dist.world, w.flops,
+                    args.steps, lambda x: dist.max(x, device))
     windows = [r["window"]]
     launches_per_step = r["launches"] / args.steps
     mean_launch_ms = statistics.mean(r["per_step_ms"])
-    bound, peak, peak_how = mode_peak(mode, peaks, num_sms)
+
+    # ---- this GPU's cuBLAS TF32 and FP8 rates: the denominators of those modes
+    measured = measure_tensor_peaks(device) if not args.quick else {}
+    bound, peak, peak_how = mode_peak(mode, peaks, num_sms, measured)
     achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
+    traffic, traffic_src = recorded_traffic(mode, w.name)
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": profiled_traffic(mode, w.name),
+                "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
                 "kernel": kernel_name(mode, w.M, w.N, num_sms),
                 "peak_source": f"{peak_src}: {peak_how}",
-                "per_launch_flops": w.flops, "launches_per_step": launches_per_step}
+                "per_launch_flops": w.flops, "launches_per_step": launches_per_step,
+                "achieved_from": "2MNK / mean per-launch device time (CUDA events, timed steps)"}
+    if bound == "tensor":
+        roofline["peak_nominal_ratio"] = round(nominal_peak(mode, peaks), 1)
+        roofline["frac_of_nominal_ratio"] = round(achieved / nominal_peak(mode, peaks), 4)
+    if measured.get("errors"):
+        roofline["peak_measure_errors"] = measured["errors"]
 
     # ---- cuBLAS on the same operands (comparator for the roofline fraction)
+    cublas_head = (None, "not timed")
     if not args.quick and not ta and not tb and dist.world == 1:
-        ms_cublas = cublas_same_run(mode, Ad, Bd, device)
-        if ms_cublas:
-            tf = w.flops / (ms_cublas * 1e-3) / 1e12
-            roofline["cublas_same_run"] = {"tflops": round(tf, 1),
-                                           "frac_of_cublas": round(achieved / tf, 4)}
+        cublas_head = cublas_same_run(mode, Ad, Bd, device)
+        roofline["cublas_same_run"] = cublas_entry(w.flops, achieved, *cublas_head)
 
     # ---- end to end through the public API with host buffers
     e2e_line = None
@@ -693,12 +788,13 @@ def run_ours(args, dist):
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
         e2e_ms, h2d, d2h = time_e2e(mode, A, B, e2e_steps, 3, dist, device)
-        e2e = aggregate(e2e_ms, dist.world, w.flops, e2e_steps, lambda x: dist.max(x, device))
-        e2e_line = {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = aggregate(e2e_ms / e2e_steps, e2e_ms, dist.world, w.flops, e2e_steps,
+                        lambda x: dist.max(x, device))
+        e2e_line = {"value": e2e["value_from_total"], "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h}
     torch.cuda.empty_cache()
 
-    # ---- every other mode, same clocking
+    # ---- every other mode, same clocking, each with cuBLAS on its operands
     modes = {}
     if not args.no_modes:
         table = [("simt", False), ("tf32", False), ("3xtf32", False), ("bf16", True),
@@ -707,24 +803,30 @@ def run_ours(args, dist):
             wm = workload_for(m, transformer=tr)
             if m == mode and wm.name == w.name:
                 per = r["per_step_ms"]
+                cub = cublas_head
             else:
                 _, _, Adm, Bdm = device_inputs(wm, m, device)
                 Cm = torch.empty((wm.M, wm.N), dtype=torch.float32, device=device)
-                steps_m = 2 if args.quick else max(5, min(args.steps, 20))
+                steps_m = 2 if args.quick else max(20, min(args.steps, 30))
                 rm = time_device(m, Adm, Bdm, Cm, steps_m, 3, dist, device)
                 windows.append(rm["window"])
                 per = rm["per_step_ms"]
+                cub = ((None, "not timed") if args.quick or dist.world > 1
+                       else cublas_same_run(m, Adm, Bdm, device))
                 del Adm, Bdm, Cm
                 torch.cuda.empty_cache()
-            bm, pm, _ = mode_peak(m, peaks, num_sms)
+            bm, pm, how = mode_peak(m, peaks, num_sms, measured)
             med = statistics.median(per)
             tfl = wm.flops / (med * 1e-3) / 1e12
-            modes[f"{m}@{wm.name}"] = {"tflops_median": round(tfl, 2), "bound": bm,
-                                       "peak": round(pm, 1), "frac": round(tfl / pm, 4),
-                                       "ms_median": round(med, 4), "ms_min": round(min(per), 4),
-                                       "ms_max": round(max(per), 4), "steps": len(per)}
+            e = {"tflops_median": round(tfl, 2), "bound": bm, "peak": round(pm, 1),
+                 "frac": round(tfl / pm, 4), "peak_source": how, "ms_median": round(med, 4),
+                 "ms_min": round(min(per), 4), "ms_max": round(max(per), 4), "steps": len(per),
+                 "cublas_same_run": cublas_entry(wm.flops, tfl, *cub)}
             if m == "3xtf32":  # three TF32 products per product: the tensor pipe's share
-                modes[f"{m}@{wm.name}"]["mma_frac"] = round(3 * tfl / pm, 4)
+                e["mma_frac"] = round(3 * tfl / pm, 4)
+            if m == "simt":
+                e["kernel"] = kernel_name(m, wm.M, wm.N, num_sms)
+            modes[f"{m}@{wm.name}"] = e
     small = {}
     if not args.no_modes and not args.shape:
         small, sw = time_small(device, dist)
@@ -763,7 +865,12 @@ def run_ours(args, dist):
             "modes": modes,
             "small": small,
             "step_ms": {"median": statistics.median(r["per_step_ms"]),
-                        "min": min(r["per_step_ms"]), "max": max(r["per_step_ms"])},
+                        "min": min(r["per_step_ms"]), "max": max(r["per_step_ms"]),
+                        "mean": mean_launch_ms, "total_of_k_steps": agg["ms_total"],
+                        "value_from_total": agg["value_from_total"],
+                        "value_is": "whole-job TFLOP/s over the median of the K timed steps"},
+            "measured_peaks_this_run": {k: (round(v, 1) if isinstance(v, float) else v)
+                                        for k, v in measured.items()},
         }
         print(json.dumps(line), flush=True)
     st, where = dg.dgemm_watchdog_status(torch.cuda.current_stream(device).cuda_stream)

@@ -15,6 +15,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -137,14 +138,23 @@ int validate(int M, int N, int K, bool a_t, bool b_t, const void *A, int lda, co
 
 // ------------------------------------------------------------------------
 // Scratch: a library-owned stream-ordered memory pool per device.  Freed
-// scratch stays reserved in the pool (up to kPoolKeepBytes) so that the next
-// call's allocation is a pool hit instead of a trip to the driver; 1 GiB
-// holds the lo parts of 3xTF32 operands up to 16384 x 8192 each.
+// scratch is reused by the next allocations on the stream; at the next
+// synchronisation the pool returns what it holds beyond its release threshold
+// to the system, so at most kPoolKeepBytes (32 MiB: the re-pitched operands of
+// the small workloads, the SIMT tail split's partial tiles at 8192^3) stays
+// reserved between calls.  DGEMM_POOL_KEEP_BYTES overrides the bound (read
+// once per device, when its pool is created).
 namespace dg {
 namespace {
-constexpr uint64_t kPoolKeepBytes = 1ull << 30;
+constexpr uint64_t kPoolKeepBytes = 32ull << 20;
 std::mutex g_pool_mutex;
 cudaMemPool_t g_pools[64] = {};
+
+uint64_t pool_keep_bytes() {
+  const char *e = getenv("DGEMM_POOL_KEEP_BYTES");
+  if (e == nullptr || e[0] < '0' || e[0] > '9') return kPoolKeepBytes;
+  return strtoull(e, nullptr, 10);
+}
 }  // namespace
 
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
@@ -162,7 +172,7 @@ cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
       props.location.id = dev;
       cudaMemPool_t p = nullptr;
       if ((e = cudaMemPoolCreate(&p, &props)) != cudaSuccess) return e;
-      uint64_t keep = kPoolKeepBytes;
+      uint64_t keep = pool_keep_bytes();
       if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
         cudaMemPoolDestroy(p);
         return e;

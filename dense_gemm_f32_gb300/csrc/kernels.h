@@ -90,7 +90,8 @@ cudaError_t launch_split_lo(const float *A, int64_t lda, float *A_lo, int a_rows
 bool tc_use_pair(int M, int N, int num_sms);
 
 // Stream-ordered scratch from the library's memory pool on the current device
-// (freed scratch stays reserved in the pool for reuse, up to 1 GiB).
+// (freed scratch is reused by later allocations; at a synchronisation the pool
+// keeps at most its release threshold, 32 MiB by default, reserved).
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);
 cudaError_t scratch_free(void *ptr, cudaStream_t stream);
 

@@ -44,10 +44,14 @@
  *     per-thread error string and a per-device watchdog word (see
  *     dgemm_watchdog_status).
  *   - Some paths use temporary device memory (re-pitched operands, the FP32
- *     SIMT path's K-split partials, the lo parts of 3xTF32 operands):
- *     stream-ordered allocations on `stream` from a memory pool the library
- *     creates per device, which keeps up to 1 GiB of freed scratch reserved
- *     for the next calls.
+ *     SIMT path's K-split partials, the lo parts of 3xTF32 operands, 8-bit
+ *     transposes): stream-ordered allocations on `stream`, freed on `stream`
+ *     at the end of the call, from a memory pool the library creates per
+ *     device.  Back-to-back calls reuse the pool's memory; at the next
+ *     stream, event or device synchronisation the pool returns what it holds
+ *     beyond 32 MiB to the system, so no more than 32 MiB stays reserved
+ *     between calls.  DGEMM_POOL_KEEP_BYTES (read once, when the pool is
+ *     created) sets another bound, e.g. 0 to keep nothing.
  */
 #ifndef DGEMM_H
 #define DGEMM_H

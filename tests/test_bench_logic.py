@@ -1,6 +1,6 @@
 """bench.py host logic on the CPU: whole-job aggregation over ranks (gloo,
 world size 2), clock summaries, argument rules, the reference arm's rank
-handling, and the traffic table lookup."""
+handling, the roofline denominators and the traffic table lookup."""
 import json
 import os
 import socket
@@ -15,9 +15,11 @@ import bench  # noqa: E402
 
 
 def test_aggregate_single_rank():
-    r = bench.aggregate(10.0, 1, 2e12, 5, lambda x: x)
-    assert r["ms_per_step"] == pytest.approx(2.0)
-    assert r["value"] == pytest.approx(5 * 2e12 / 1e-2 / 1e12)
+    """value from the median step; value_from_total from the K steps' total."""
+    r = bench.aggregate(1.9, 10.0, 1, 2e12, 5, lambda x: x)
+    assert r["ms_per_step"] == pytest.approx(1.9)
+    assert r["value"] == pytest.approx(2e12 / 1.9e-3 / 1e12)
+    assert r["value_from_total"] == pytest.approx(5 * 2e12 / 1e-2 / 1e12)
 
 
 def _free_port():
@@ -32,7 +34,7 @@ def _rank_main(rank, world, port, local_ms, q):
     d = bench.Dist()
     d.init("gloo")
     d.barrier()
-    r = bench.aggregate(local_ms[rank], d.world, 1e12, 4, d.max)
+    r = bench.aggregate(local_ms[rank] / 4 - rank * 0.1, local_ms[rank], d.world, 1e12, 4, d.max)
     q.put((rank, r))
     d.close()
 
@@ -51,8 +53,11 @@ def test_aggregate_two_ranks_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     for r in (0, 1):
+        # medians 2.0 (rank 0) and 2.9 (rank 1): the slowest rank's median counts
         assert out[r]["ms_total"] == pytest.approx(12.0)
-        assert out[r]["value"] == pytest.approx(2 * 1e12 * 4 / 12e-3 / 1e12)
+        assert out[r]["ms_per_step"] == pytest.approx(2.9)
+        assert out[r]["value"] == pytest.approx(2 * 1e12 / 2.9e-3 / 1e12)
+        assert out[r]["value_from_total"] == pytest.approx(2 * 1e12 * 4 / 12e-3 / 1e12)
 
 
 def test_clock_summary_inside_windows():
@@ -97,25 +102,34 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
 
 
 def test_mode_peaks():
+    """Measured cuBLAS rates of this run take precedence for TF32 (and 3xTF32)
+    and FP8; without them the BF16 burst times the nominal ratio."""
     peaks = {"bf16_tflops": 2000.0, "sm_max_mhz": 2000.0}
     assert bench.mode_peak("bf16", peaks, 100)[1] == 2000.0
     assert bench.mode_peak("tf32", peaks, 100)[1] == pytest.approx(2000.0 * 1.1 / 2.25)
+    b, p, how = bench.mode_peak("tf32", peaks, 100, {"tf32": 1040.0, "fp8": 3500.0})
+    assert p == 1040.0 and how.startswith("measured in this run")
+    assert bench.mode_peak("3xtf32", peaks, 100, {"tf32": 1040.0})[1] == 1040.0
+    assert bench.mode_peak("e5m2", peaks, 100, {"fp8": 3500.0})[1] == 3500.0
+    assert bench.mode_peak("e4m3", peaks, 100, {"tf32": 1040.0})[2].startswith("fallback")
+    assert bench.nominal_peak("e4m3", peaks) == pytest.approx(4000.0)
     b, p, _ = bench.mode_peak("simt", peaks, 100)
     assert b == "alu" and p == pytest.approx(100 * 128 * 2 * 2000e6 / 1e12)
 
 
-def test_traffic_table_respects_source_hash(tmp_path, monkeypatch):
-    prof = tmp_path / "profiles"
-    prof.mkdir()
+def test_traffic_table_respects_source_hash():
+    """A recorded DRAM-traffic figure applies only to the sources it was
+    captured on; otherwise the line carries null and says why."""
     sha = bench.source_sha("tf32")
-    (prof / "dram_traffic.md").write_text(
-        "| mode | workload | source | bytes |\n|---|---|---|---|\n"
-        f"| tf32 | w1 | {sha} | 1234 |\n| simt | w1 | 000000000000 | 99 |\n")
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    (tmp_path / "dense_gemm_f32_gb300").symlink_to(os.path.join(ROOT, "dense_gemm_f32_gb300"))
-    assert bench.profiled_traffic("tf32", "w1") == 1234.0
-    assert bench.profiled_traffic("simt", "w1") is None
-    assert bench.profiled_traffic("tf32", "other") is None
+    table = {("tf32", "w1"): {"bytes": 1234, "sha": sha, "command": "ncu ..."},
+             ("simt", "w1"): {"bytes": 99, "sha": "000000000000", "command": "ncu ..."}}
+    v, src = bench.recorded_traffic("tf32", "w1", table)
+    assert v == 1234.0 and src["command"] == "ncu ..."
+    v, why = bench.recorded_traffic("simt", "w1", table)
+    assert v is None and "stale" in why
+    v, why = bench.recorded_traffic("tf32", "other", table)
+    assert v is None and "no ncu capture" in why
+    assert bench.source_sha("simt") != sha
 
 
 def test_reference_line_shape(capsys):
