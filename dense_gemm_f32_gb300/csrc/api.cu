@@ -262,18 +262,20 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
     e = dg::scratch_alloc(&scratch, a_bytes + b_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "scratch allocation (re-pitch)");
     char *s = static_cast<char *>(scratch);
+    dg::RepitchJob jobs[2];
+    int njobs = 0;
     if (!a_ok) {
-      e = dg::launch_repitch(A, lda, s, lda2, a_rows, a_cols, es, num_sms, stream);
-      if (e != cudaSuccess) goto done;
+      jobs[njobs++] = {A, lda, s, lda2, a_rows, a_cols};
       Ause = s;
       lda_use = lda2;
     }
     if (!b_ok) {
-      e = dg::launch_repitch(B, ldb, s + a_bytes, ldb2, b_rows, b_cols, es, num_sms, stream);
-      if (e != cudaSuccess) goto done;
+      jobs[njobs++] = {B, ldb, s + a_bytes, ldb2, b_rows, b_cols};
       Buse = s + a_bytes;
       ldb_use = ldb2;
     }
+    e = dg::launch_repitch(jobs, njobs, es, num_sms, stream);  // both operands, one launch
+    if (e != cudaSuccess) goto done;
   }
   {
     // 3xTF32 on the CTA-pair kernel: the split pre-pass writes lo(A) and
@@ -355,18 +357,20 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
     const int st = noalloc_scratch(dev, &base);
     if (st != DGEMM_OK) return st;
     char *s = static_cast<char *>(base);
+    dg::RepitchJob jobs[2];
+    int njobs = 0;
     if (!a_ok) {
-      e = dg::launch_repitch(A, lda, s, lda2, M, K, es, num_sms, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "re-pitch launch (no-alloc)");
+      jobs[njobs++] = {A, lda, s, lda2, M, K};
       Ause = s;
       lda_use = lda2;
     }
     if (!b_ok) {
-      e = dg::launch_repitch(B, ldb, s + a_bytes, ldb2, K, N, es, num_sms, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "re-pitch launch (no-alloc)");
+      jobs[njobs++] = {B, ldb, s + a_bytes, ldb2, K, N};
       Buse = s + a_bytes;
       ldb_use = ldb2;
     }
+    e = dg::launch_repitch(jobs, njobs, es, num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "re-pitch launch (no-alloc)");
   }
   // 3xTF32 on the CTA-pair kernel when the lo parts fit in the rest of the
   // fixed scratch; otherwise the single-CTA kernel splits in shared memory.

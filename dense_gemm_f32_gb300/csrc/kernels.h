@@ -69,10 +69,19 @@ cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t l
                               int cols, int num_sms, cudaStream_t stream);
 
 // Copy a rows x cols matrix of elem_bytes-sized elements (4, 2 or 1) from
-// (src, lds) to (dst, ldd); used to re-pitch operands whose rows do not start
-// on 16-byte boundaries.
-cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
-                           int cols, int elem_bytes, int num_sms, cudaStream_t stream);
+// (src, lds) to (dst, ldd), the padding columns up to ldd zeroed; used to
+// re-pitch operands whose rows do not start on 16-byte boundaries (dst
+// 16-byte aligned, ldd * elem_bytes a multiple of 16).  Up to two jobs (A and
+// B) go out in one launch.
+struct RepitchJob {
+  const void *src;
+  int64_t lds;
+  void *dst;
+  int64_t ldd;
+  int rows, cols;
+};
+cudaError_t launch_repitch(const RepitchJob *jobs, int njobs, int elem_bytes, int num_sms,
+                           cudaStream_t stream);
 
 // 3xTF32 split pre-pass: A_lo = lo(A) (a_rows x a_cols, leading dimension
 // lda) and B_lo = lo(B) likewise, lo(x) = x - trunc_tf32(x) rounded to TF32

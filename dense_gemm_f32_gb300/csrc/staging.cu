@@ -18,16 +18,31 @@
 namespace dg {
 namespace {
 
-__global__ void repitch_kernel(const uint8_t *__restrict__ src, int64_t lds_bytes,
-                               uint8_t *__restrict__ dst, int64_t ldd_bytes, int rows,
-                               int64_t row_bytes, int es) {
+// One operand of a re-pitch launch.
+struct RepitchOp {
+  const uint8_t *src;
+  uint8_t *dst;
+  int64_t lds_bytes, ldd_bytes, row_bytes;
+  int rows;
+};
+
+__global__ void repitch_kernel(RepitchOp op0, RepitchOp op1, int es) {
   // One 16-byte destination chunk per thread-iteration (dst rows are
   // 16-byte aligned, ldd_bytes a multiple of 16): 16 / es element loads from
   // the unaligned source row, one 128-bit store; columns past the row are
   // zeroed.  Rows run along y, chunks along x, so there is no division per
-  // element.
+  // element; the operand is grid z (chosen field by field: indexing a
+  // parameter array with blockIdx.z would copy the parameters to local memory
+  // in every thread).
   pdl_launch_dependents();
   pdl_wait();
+  const bool second = blockIdx.z != 0;
+  const uint8_t *__restrict__ src = second ? op1.src : op0.src;
+  uint8_t *__restrict__ dst = second ? op1.dst : op0.dst;
+  const int64_t lds_bytes = second ? op1.lds_bytes : op0.lds_bytes;
+  const int64_t ldd_bytes = second ? op1.ldd_bytes : op0.ldd_bytes;
+  const int64_t row_bytes = second ? op1.row_bytes : op0.row_bytes;
+  const int rows = second ? op1.rows : op0.rows;
   const int64_t chunks = ldd_bytes / 16;
   for (int r = blockIdx.y; r < rows; r += gridDim.y) {
     const uint8_t *srow = src + (int64_t)r * lds_bytes;
@@ -168,20 +183,32 @@ cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t l
   return e;
 }
 
-cudaError_t launch_repitch(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
-                           int cols, int elem_bytes, int num_sms, cudaStream_t stream) {
-  if (rows <= 0) return cudaSuccess;
-  const int64_t chunks = ldd * elem_bytes / 16;
-  const int bx = (int)((chunks + 255) / 256 < 8 ? (chunks + 255) / 256 : 8);
-  int64_t by = (int64_t)num_sms * 16 / bx;
-  if (by > rows) by = rows;
+cudaError_t launch_repitch(const RepitchJob *jobs, int njobs, int elem_bytes, int num_sms,
+                           cudaStream_t stream) {
+  RepitchOp ops[2] = {};
+  int n = 0, max_rows = 0;
+  int64_t max_chunks = 0;
+  for (int j = 0; j < njobs && j < 2; ++j) {
+    if (jobs[j].rows <= 0) continue;
+    RepitchOp &o = ops[n++];
+    o.src = static_cast<const uint8_t *>(jobs[j].src);
+    o.dst = static_cast<uint8_t *>(jobs[j].dst);
+    o.lds_bytes = jobs[j].lds * elem_bytes;
+    o.ldd_bytes = jobs[j].ldd * elem_bytes;
+    o.row_bytes = (int64_t)jobs[j].cols * elem_bytes;
+    o.rows = jobs[j].rows;
+    const int64_t chunks = o.ldd_bytes / 16;
+    max_chunks = chunks > max_chunks ? chunks : max_chunks;
+    max_rows = o.rows > max_rows ? o.rows : max_rows;
+  }
+  if (n == 0) return cudaSuccess;
+  const int bx = (int)((max_chunks + 255) / 256 < 8 ? (max_chunks + 255) / 256 : 8);
+  int64_t by = (int64_t)num_sms * 16 / (bx * n);
+  if (by > max_rows) by = max_rows;
   if (by > 65535) by = 65535;
   if (by < 1) by = 1;
-  const cudaError_t e = launch_kernel(repitch_kernel, dim3((unsigned)bx, (unsigned)by), dim3(256), 0,
-                                      stream, 1, static_cast<const uint8_t *>(src),
-                                      lds * elem_bytes, static_cast<uint8_t *>(dst),
-                                      ldd * elem_bytes, rows, (int64_t)cols * elem_bytes,
-                                      elem_bytes);
+  const cudaError_t e = launch_kernel(repitch_kernel, dim3((unsigned)bx, (unsigned)by, (unsigned)n),
+                                      dim3(256), 0, stream, 1, ops[0], ops[1], elem_bytes);
   if (e == cudaSuccess) count_launch();
   return e;
 }

@@ -96,7 +96,7 @@ enum : int {
 // AT: A is stored K x M (op(A) = A^T), read MN-major.  BT: B is stored N x K
 // (op(B) = B^T), read K-major.  The defaults are the row-major A (K-major)
 // and B (MN-major) of the plain product.
-template <TcKind KIND, int BN_, bool AT_ = false, bool BT_ = false>
+template <TcKind KIND, int BN_, bool AT_ = false, bool BT_ = false, int BUDGET_ = 196608>
 struct Cfg {
   static constexpr bool AT = AT_, BT = BT_;
   // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
@@ -128,7 +128,9 @@ struct Cfg {
   static constexpr int B_BOX_BYTES = BT ? B_BYTES : BK * 128;
   static constexpr int RAW_BYTES = A_BYTES + B_BYTES;               // what TMA writes
   static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);  // + lo copies
-  static constexpr int STAGES = (kSplit ? 196608 : 196608) / STAGE_BYTES;
+  // stages that fit the shared-memory budget: 192 KB (one CTA per SM), or
+  // 96 KB for the small-problem configuration (two CTAs per SM)
+  static constexpr int STAGES = BUDGET_ / STAGE_BYTES;
   static constexpr int ACC_COLS = 2 * BN;                           // two fp32 accumulators
   static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64
                                    : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
@@ -138,6 +140,10 @@ struct Cfg {
   // barriers: full[S], empty[S], split[S], acc_full[2], acc_empty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 6;  // + the test-stall barrier
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
+  // CTAs that fit on one SM (228 KB of shared memory, 1 KB reserved per CTA;
+  // 512 TMEM columns)
+  static constexpr int CTAS_PER_SM =
+      (2 * (SMEM_BYTES + 1024) <= 233472 && 2 * TMEM_COLS <= 512) ? 2 : 1;
   // K-split: the partial 128 x BN tile parked in the (then idle) stage area,
   // rows padded by 4 floats so that the epilogue's 16-byte row stores from 8
   // consecutive lanes fall in distinct banks.
@@ -212,13 +218,13 @@ __device__ __forceinline__ void watchdog_trip(int *watchdog, int site, volatile 
   *abort_flag = 1;
 }
 
-template <TcKind KIND, int BN, bool AT, bool BT>
-__global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT>::THREADS, 1)
+template <TcKind KIND, int BN, bool AT, bool BT, int BUDGET>
+__global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
                    int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
                    int splits, int mn3d, int stall) {
-  using G = Cfg<KIND, BN, AT, BT>;
+  using G = Cfg<KIND, BN, AT, BT, BUDGET>;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -1055,6 +1061,27 @@ int snake_order(bool dflt) {
   return dflt ? 1 : 0;
 }
 
+// Small-problem configuration of the single-CTA kernel: 128 x 128 tiles and
+// 3 stages (96 KB of stages, 256 TMEM columns), so that two CTAs fit on an
+// SM: the next call's CTAs can then start their set-up beside the previous
+// call's (programmatic dependent launch), and each CTA writes half the C of a
+// 128 x 256 tile.  Measured on GB300 (graph replay, same process, against the
+// 128 x 256 4-stage configuration): ahead for 8-bit operands at every small
+// shape tried (1024^3 E4M3 12.5 -> 9.4 us, 2048 x 1024 x 1024 12.8 -> 8.9 us)
+// and for every kind when K is short (64^3 TF32 3.9 -> 3.2 us, 1024 x 1024 x
+// 256 TF32 10.3 -> 8.3 us); behind for 32- and 16-bit operands with longer K
+// (1024^3 TF32 10.7 -> 12.0 us, 1024 x 1024 x 4096 TF32 18.1 -> 28.6 us),
+// where the wider tile's lower operand traffic per flop wins.  So it runs for
+// 8-bit operands, and for the others when a row of K is at most 1 KB.
+// DGEMM_TC_SMALL=0 / =1 forces it off / on (read at every launch, for tests
+// and tuning).  3xTF32 keeps its own 128 x 128 configuration with split warps.
+constexpr int kSmallBudget = 3 * 32768;
+bool tc_small_config(int elem_bytes, int K) {
+  const char *e = getenv("DGEMM_TC_SMALL");
+  if (e && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+  return elem_bytes == 1 || (int64_t)K * elem_bytes <= 1024;
+}
+
 // DGEMM_TC_TEST_STALL=1 makes the MMA thread of the first CTA (pair) wait on
 // a barrier that nothing arrives at: its bounded wait runs out after ~2 s and
 // the kernel takes its abort path (watchdog site code, drained copies, freed
@@ -1160,7 +1187,7 @@ int active_clusters(Kern kern, int threads, int smem, int dev, int size) {
 // clusters that do not fit run in waves), for tests and tuning.
 template <class Kern>
 int choose_splits(Kern kern, int threads, int smem, int dev, int64_t tiles, int kblocks,
-                  int num_sms) {
+                  int slots) {
   auto whole = [&](int s) {  // parts actually used when aiming for s
     const int per = (kblocks + s - 1) / s;
     return (kblocks + per - 1) / per;
@@ -1170,8 +1197,8 @@ int choose_splits(Kern kern, int threads, int smem, int dev, int64_t tiles, int 
     const int f = env[0] - '0';
     return f >= 2 && kblocks >= 2 ? whole(f < kblocks ? f : kblocks) : 1;
   }
-  if (tiles * 2 > num_sms) return 1;
-  int s = (int)(num_sms / tiles);
+  if (tiles * 2 > slots) return 1;
+  int s = (int)(slots / tiles);
   s = s < 8 ? s : 8;
   s = s < kblocks / 4 ? s : kblocks / 4;
   for (; s >= 2; --s) {
@@ -1181,16 +1208,16 @@ int choose_splits(Kern kern, int threads, int smem, int dev, int64_t tiles, int 
   return 1;
 }
 
-template <TcKind KIND, int BN, bool AT, bool BT>
+template <TcKind KIND, int BN, bool AT, bool BT, int BUDGET = 196608>
 cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
                        int *watchdog, cudaStream_t stream) {
-  using G = Cfg<KIND, BN, AT, BT>;
+  using G = Cfg<KIND, BN, AT, BT, BUDGET>;
   CUtensorMap ta, tb;
   int mn3d = 0;
   if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN, &mn3d))
     return cudaErrorInvalidValue;
-  auto kern = tc_gemm_kernel<KIND, BN, AT, BT>;
+  auto kern = tc_gemm_kernel<KIND, BN, AT, BT, BUDGET>;
   static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1203,10 +1230,12 @@ cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const vo
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int kblocks = (K + G::BK - 1) / G::BK;
-  const int splits = choose_splits(kern, G::THREADS, G::SMEM_BYTES, dev, tiles, kblocks, num_sms);
+  const int64_t slots = (int64_t)num_sms * G::CTAS_PER_SM;
+  const int splits = choose_splits(kern, G::THREADS, G::SMEM_BYTES, dev, tiles, kblocks,
+                                   (int)slots);
   // K-split: one unit per CTA, the `splits` parts of a tile in one cluster;
-  // else a persistent grid of at most one CTA per SM.
-  const int64_t grid = splits > 1 ? tiles * splits : (tiles < num_sms ? tiles : num_sms);
+  // else a persistent grid of at most CTAS_PER_SM CTAs per SM.
+  const int64_t grid = splits > 1 ? tiles * splits : (tiles < slots ? tiles : slots);
   e = launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream,
                     splits > 1 ? (unsigned)splits : 1u, ta, tb, C, M, N, K, ldc, c_vec ? 1 : 0,
                     raster_group_m(32), watchdog, splits, mn3d, test_stall());
@@ -1288,6 +1317,11 @@ cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const v
   if (lo_ok && tc_use_pair(M, N, num_sms))
     return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream,
                                      A_lo, B_lo);
+  if constexpr (KIND != TcKind::k3xTF32) {
+    if (tc_small_config(Cfg<KIND, BN1, AT, BT>::ES, K))
+      return launch_cfg<KIND, 128, AT, BT, kSmallBudget>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
+                                                          num_sms, watchdog, stream);
+  }
   return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog, stream);
 }
 
