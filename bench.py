@@ -219,7 +219,33 @@ def source_sha(mode):
 # launch), keyed by (mode, workload); `sha` is source_sha(mode) of the sources
 # the capture ran, so a figure goes stale (null in the line) as soon as the
 # kernel changes.  The summaries of these captures are in profiles/.
-RECORDED_TRAFFIC = {}
+_NCU = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+        "--clock-control none -k regex:{k} -s 3 -c 1 python bench.py --mode {m} --steps 3 "
+        "--warmup 3 --no-modes --no-cpu --no-e2e")
+_WHERE = "one GB300 of the pool, 2026-12-02, after the same command exited 0 without ncu"
+RECORDED_TRAFFIC = {
+    ("tf32", "square-8192 fp32"): {
+        "bytes": 2050968576 + 258755328, "sha": "e3ec734d5641", "kernel": "tc2_gemm_kernel<TF32>",
+        "read": 2050968576, "write": 258755328, "command": _NCU.format(k="tc2_gemm", m="tf32"),
+        "where": _WHERE},
+    ("3xtf32", "square-8192 fp32"): {
+        "bytes": 4318036480 + 262111488, "sha": "e3ec734d5641",
+        "kernel": "tc2_gemm_kernel<3xTF32> (lo parts loaded too)", "read": 4318036480,
+        "write": 262111488, "command": _NCU.format(k="tc2_gemm", m="3xtf32"), "where": _WHERE},
+    ("bf16", "transformer-layer 16384x14336x4096 bf16"): {
+        "bytes": 1024661248 + 907866368, "sha": "e3ec734d5641", "kernel": "tc2_gemm_kernel<BF16>",
+        "read": 1024661248, "write": 907866368, "command": _NCU.format(k="tc2_gemm", m="bf16"),
+        "where": _WHERE},
+    ("e4m3", "transformer-layer 16384x14336x4096 e4m3"): {
+        "bytes": 311126272 + 888528640, "sha": "e3ec734d5641",
+        "kernel": "tc2_gemm_kernel<E4M3> (B stored N x K after the transpose launch)",
+        "read": 311126272, "write": 888528640, "command": _NCU.format(k="tc2_gemm", m="e4m3"),
+        "where": _WHERE},
+    ("simt", "square-8192 fp32"): {
+        "bytes": 2855109632 + 262675456, "sha": "a022c02811ef", "kernel": "sgemm_ring_kernel",
+        "read": 2855109632, "write": 262675456, "command": _NCU.format(k="sgemm_ring", m="simt"),
+        "where": _WHERE},
+}
 
 
 def recorded_traffic(mode, workload_name, table=None):
@@ -779,7 +805,9 @@ def run_ours(args, dist):
     cublas_head = (None, "not timed")
     if not args.quick and not ta and not tb and dist.world == 1:
         cublas_head = cublas_same_run(mode, Ad, Bd, device)
-        roofline["cublas_same_run"] = cublas_entry(w.flops, achieved, *cublas_head)
+        # like with like: our median step against cuBLAS's median call
+        median_tflops = w.flops / (statistics.median(r["per_step_ms"]) * 1e-3) / 1e12
+        roofline["cublas_same_run"] = cublas_entry(w.flops, median_tflops, *cublas_head)
 
     # ---- end to end through the public API with host buffers
     e2e_line = None
