@@ -482,16 +482,19 @@ struct RingCfg {
   static constexpr int PART_PITCH = BN + 4;
   static constexpr int PART_BYTES = BM * PART_PITCH * 4;
   static constexpr int DATA_BYTES = RING_BYTES > PART_BYTES ? RING_BYTES : PART_BYTES;
-  // full and empty barriers, the count of issued k-blocks, the abort flag
-  static constexpr int TAIL_BYTES = 2 * STAGES * 8 + 8;
+  // full and empty barriers, the test-stall barrier, the count of issued
+  // k-blocks, the abort flag
+  static constexpr int TAIL_BYTES = (2 * STAGES + 1) * 8 + 8;
   static constexpr int SMEM_BYTES = 1024 + DATA_BYTES + TAIL_BYTES;  // 1024: alignment slack
 };
 
-// Watchdog site codes of the ring kernel (role * 16 + place).
+// Watchdog site codes of the ring kernel (distinct from the tensor-core
+// kernels' codes).
 enum : int {
-  kSiteRingFull = 0x51,   // a warp's wait for a stage's copy
-  kSiteRingEmpty = 0x52,  // a refill's wait for the warps to release a stage
-  kSiteRingDrain = 0x53,  // the wait for copies still in flight after an abort
+  kSiteRingFull = 0x81,       // a warp's wait for a stage's copy
+  kSiteRingEmpty = 0x82,      // a refill's wait for the warps to release a stage
+  kSiteRingDrain = 0x83,      // the wait for copies still in flight after an abort
+  kSiteRingTestStall = 0x84,  // DGEMM_SIMT_TEST_STALL: warp 0 of CTA 0's test wait ran out
 };
 
 template <class G, bool AT>
@@ -500,7 +503,8 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
                       const __grid_constant__ CUtensorMap tmap_b, int M, int N, int K,
                       float *__restrict__ C, int64_t ldc, int c_vec, int split_first,
                       int split_parts, float *__restrict__ work,
-                      unsigned int *__restrict__ counters, int cluster_parts, int *watchdog) {
+                      unsigned int *__restrict__ counters, int cluster_parts, int *watchdog,
+                      int stall) {
   constexpr int BM = G::BM, BN = G::BN, BK = G::BK, TM = G::TM, TN = G::TN, S = G::STAGES;
   pdl_launch_dependents();
   extern __shared__ uint8_t ring_smem_raw[];
@@ -510,7 +514,8 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   const uint32_t bars = base + G::DATA_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
-  int *issued = reinterpret_cast<int *>(smem + G::DATA_BYTES + 16 * S);
+  const uint32_t stall_bar = bars + 8u * (2 * S);  // nothing ever arrives here
+  int *issued = reinterpret_cast<int *>(smem + G::DATA_BYTES + 8 * (2 * S + 1));
   volatile int *abort_flag = issued + 1;
 
   // ---- work unit -> (tile, K range), as in sgemm_simt_kernel
@@ -542,6 +547,7 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), G::NWARPS);
     }
+    mbar_init(stall_bar, 1);
     *issued = 0;
     *abort_flag = 0;
     fence_mbar_init();
@@ -606,7 +612,16 @@ __global__ void __launch_bounds__(G::THREADS, G::MIN_BLOCKS)
   };
   auto comp = [](const float4 &v, int t) { return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w; };
 
-  for (int it = 0; it < nkb; ++it) {
+  if (stall && blockIdx.x == 0 && warp == 0) {
+    // Test hook: wait on a barrier that nothing arrives at, so that the
+    // bounded wait runs out and the abort path below runs for real.
+    const bool got = mbar_wait(stall_bar, 0);
+    if (!__all_sync(0xffffffffu, got) && lane == 0) {
+      atomicCAS(watchdog, 0, kSiteRingTestStall);
+      *abort_flag = 1;
+    }
+  }
+  for (int it = 0; it < nkb && !(stall && blockIdx.x == 0 && warp == 0); ++it) {
     const int s = it % S;
     const uint32_t ph = (uint32_t)(it / S) & 1u;
     bool got = mbar_try_wait(full_bar(s), ph) || (!*abort_flag && mbar_wait(full_bar(s), ph));
@@ -808,6 +823,15 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
       });
 }
 
+// DGEMM_SIMT_TEST_STALL=1 makes warp 0 of the ring kernel's first CTA wait on
+// a barrier that nothing arrives at: the wait runs out after ~2 s and the
+// kernel takes its abort path (watchdog site code, drained copies,
+// incomplete C).  For the failure-detection test only; read at every launch.
+int simt_test_stall() {
+  const char *e = getenv("DGEMM_SIMT_TEST_STALL");
+  return (e && e[0] == '1') ? 1 : 0;
+}
+
 // The TMA ring kernel for A stored M x K (AT = false) or K x M and B stored
 // K x N, both with 16-byte aligned rows.
 template <class G, bool AT>
@@ -839,7 +863,8 @@ cudaError_t launch_ring_cfg(int M, int N, int K, const float *A, int64_t lda, co
           unsigned int *counters, int cparts) {
         return launch_kernel(kern, dim3((unsigned)grid), dim3(G::THREADS), G::SMEM_BYTES, stream,
                              (unsigned)cluster, ta, tb, M, N, K, C, ldc, c_vec ? 1 : 0,
-                             (int)split_first, parts, work, counters, cparts, wd);
+                             (int)split_first, parts, work, counters, cparts, wd,
+                             simt_test_stall());
       });
 }
 

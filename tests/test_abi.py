@@ -130,9 +130,12 @@ def test_matmul_argument_checks_need_no_gpu():
 
 
 def test_watchdog_site_codes_documented():
-    src = open(os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc", "tc.cu"), encoding="utf-8").read()
-    codes = re.findall(r"kSite\w+ = (0x[0-9a-f]+)", src)
-    assert len(codes) == len(set(codes)) >= 5
+    """Every bounded wait of every kernel has its own site code, across files."""
+    codes = []
+    for f in ("tc.cu", "simt.cu"):
+        src = open(os.path.join(ROOT, "dense_gemm_f32_gb300", "csrc", f), encoding="utf-8").read()
+        codes += re.findall(r"kSite\w+ = (0x[0-9a-f]+)", src)
+    assert len(codes) == len(set(codes)) >= 9
 
 
 def _caller(fn):
