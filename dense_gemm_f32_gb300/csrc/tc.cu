@@ -139,7 +139,13 @@ struct Cfg {
   static constexpr int THREADS = 32 * (2 + kEpiWarps + kSplitWarps);
   // barriers: full[S], empty[S], split[S], acc_full[2], acc_empty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 6;  // + the test-stall barrier
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
+  // Epilogue staging: per epilogue warp 32 rows x 16 fp32 (64-byte rows,
+  // 16-byte chunks swizzled by row), so that C is written row by row.
+  static constexpr int EPI_COLS = 16;
+  static constexpr int EPI_WARP_BYTES = 32 * EPI_COLS * 4;
+  static constexpr int EPI_BYTES = kEpiWarps * EPI_WARP_BYTES;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 + 1024;  // +1024: align slack
   // CTAs that fit on one SM (228 KB of shared memory, 1 KB reserved per CTA;
   // 512 TMEM columns)
   static constexpr int CTAS_PER_SM =
@@ -156,6 +162,8 @@ struct Cfg {
   static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
   static_assert(kSplitWarp0 == kEpiWarp0 + kEpiWarps, "split warps follow the epilogue warps");
   static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage area");
+  static_assert(BM * BN * 4 <= STAGES * STAGE_BYTES, "a staged C tile fits the stage area");
+  static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
 
   // B (MN-major) layout.  16-bit operands use the plain 128-byte swizzle
   // (16-byte chunks permuted within each 128-byte row); 32-bit MN-major
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_base);
 
-  const uint32_t bars = base + G::STAGES * G::STAGE_BYTES;
+  const uint32_t bars = base + G::STAGES * G::STAGE_BYTES + G::EPI_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (G::STAGES + s); };
   auto split_bar = [&](int s) { return bars + 8u * (2 * G::STAGES + s); };
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
   auto acce_bar = [&](int b) { return bars + 8u * (3 * G::STAGES + 2 + b); };
   const uint32_t drain_bar = bars + 8u * (3 * G::STAGES + 4);
   const uint32_t stall_bar = bars + 8u * (3 * G::STAGES + 5);  // nothing ever arrives here
-  uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::NUM_BARS * 8;
+  uint8_t *tail = smem + G::STAGES * G::STAGE_BYTES + G::EPI_BYTES + G::NUM_BARS * 8;
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
 
@@ -440,8 +448,6 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int trow = quarter * 32 + lane;  // this thread's accumulator row
-      const int row = tm * BM + trow;
-      float *crow = C + (int64_t)row * ldc;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (splits > 1) {
         // K-split part: park the partial tile in shared memory.  Every MMA of
@@ -462,23 +468,151 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
         tc_fence_before();
         break;  // one unit per CTA
       }
+      // Tiles with more than 64 columns inside C go out row by row through
+      // shared memory, so that every store writes whole lines: each thread writes
+      // its accumulator row there (16-byte chunks, chunk q of row r at
+      // q ^ (r & 7) within its group of eight, so a quarter-warp's eight
+      // rows fill the 32 banks), then the warp writes C along rows: 16-byte
+      // stores, four or eight lanes to a row, when C's rows start on 16-byte
+      // boundaries, else one element per lane.  Columns and rows outside C
+      // are skipped (warp-uniform).
+      const int row0 = tm * BM + quarter * 32;  // C row of the warp's staged row 0
+      const int ncols = min(BN, N - tn * BN);   // columns of this tile inside C
+      if (ncols <= 64) {
+        // Narrow edge (at most two 32-column loads): each thread stores its
+        // own row straight from registers, the fewest steps.
+        const int row = row0 + lane;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
-        tmem_wait_ld();
-        const int col = tn * BN + c0;
-        if (row < M) {
-          if (c_vec && col + 32 <= N) {
+        for (int c0 = 0; row0 < M && c0 < ncols; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
+          tmem_wait_ld();
+          const int col = tn * BN + c0;
+          float *d = C + (int64_t)row * ldc + col;
+          if (row < M) {
+            if (c_vec && col + 32 <= N) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4 *>(crow + col + j) =
-                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(d + j) =
+                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col + j < N) d[j] = __uint_as_float(r[j]);
+            }
+          }
+        }
+      } else if (gridDim.x >= units) {
+        // One unit per CTA: after its last MMA the stage area is idle, so
+        // each warp stages all its columns (32 x BN) at once.
+        float *wb = reinterpret_cast<float *>(smem) + (warp - G::kEpiWarp0) * (32 * BN);
+#pragma unroll 1
+        for (int c0 = 0; row0 < M && c0 < ncols; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(wb + lane * BN + c0 + ((q ^ (lane & 7)) << 2)) =
+                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+        __syncwarp();
+        if (row0 < M) {
+          if (c_vec) {
+            const int q = lane & 7;
+#pragma unroll 1
+            for (int c0 = 0; c0 < ncols; c0 += 32) {
+              const int col = tn * BN + c0 + 4 * q;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int rr = 4 * i + (lane >> 3);
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(wb + rr * BN + c0 + ((q ^ (rr & 7)) << 2));
+                if (row0 + rr < M) {
+                  float *d = C + (int64_t)(row0 + rr) * ldc + col;
+                  if (col + 4 <= N) {
+                    *reinterpret_cast<float4 *>(d) = v;
+                  } else {
+                    if (col < N) d[0] = v.x;
+                    if (col + 1 < N) d[1] = v.y;
+                    if (col + 2 < N) d[2] = v.z;
+                  }
+                }
+              }
+            }
           } else {
+            const int sw = lane & 3, cq = lane >> 2;
+#pragma unroll 1
+            for (int c0 = 0; c0 < ncols; c0 += 32) {
+              const int col = tn * BN + c0 + lane;
+#pragma unroll 8
+              for (int rr = 0; rr < 32; ++rr) {
+                const float v = wb[rr * BN + c0 + ((cq ^ (rr & 7)) << 2) + sw];
+                if (row0 + rr < M && col < N) C[(int64_t)(row0 + rr) * ldc + col] = v;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(acc));
+        break;  // no further unit
+      } else {
+        // Persistent CTAs (the stage area holds the next tile's operands):
+        // through this warp's staging buffer, EPI_COLS columns at a time, two
+        // passes per 32-column TMEM load; 64-byte rows, chunk q of row r at
+        // q ^ ((r >> 1) & 3).
+        static_assert(G::EPI_COLS == 16 && BN % 32 == 0, "two staging passes per TMEM load");
+        float *ebuf = reinterpret_cast<float *>(smem + G::STAGES * G::STAGE_BYTES) +
+                      (warp - G::kEpiWarp0) * (32 * G::EPI_COLS);
+#pragma unroll 1
+        for (int c0 = 0; row0 < M && c0 < ncols; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col + j < N) crow[col + j] = __uint_as_float(r[j]);
+          for (int h = 0; h < 2; ++h) {
+            const int cc = c0 + 16 * h;  // first column of this pass, within the tile
+            if (cc >= ncols) break;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<float4 *>(ebuf + lane * 16 + ((q ^ ((lane >> 1) & 3)) << 2)) =
+                  make_float4(__uint_as_float(r[16 * h + 4 * q]),
+                              __uint_as_float(r[16 * h + 4 * q + 1]),
+                              __uint_as_float(r[16 * h + 4 * q + 2]),
+                              __uint_as_float(r[16 * h + 4 * q + 3]));
+            __syncwarp();
+            const int col0 = tn * BN + cc;
+            if (c_vec) {
+              const int q = lane & 3, col = col0 + 4 * q;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int rr = 8 * i + (lane >> 2);
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    ebuf + rr * 16 + ((q ^ ((rr >> 1) & 3)) << 2));
+                if (row0 + rr < M) {
+                  float *d = C + (int64_t)(row0 + rr) * ldc + col;
+                  if (col + 4 <= N) {
+                    *reinterpret_cast<float4 *>(d) = v;
+                  } else {
+                    if (col < N) d[0] = v.x;
+                    if (col + 1 < N) d[1] = v.y;
+                    if (col + 2 < N) d[2] = v.z;
+                  }
+                }
+              }
+            } else {
+              const int j = lane & 15, col = col0 + j;
+#pragma unroll 4
+              for (int i = 0; i < 16; ++i) {
+                const int rr = 2 * i + (lane >> 4);
+                const float v = ebuf[rr * 16 + (((j >> 2) ^ ((rr >> 1) & 3)) << 2) + (j & 3)];
+                if (row0 + rr < M && col < N) C[(int64_t)(row0 + rr) * ldc + col] = v;
+              }
+            }
+            __syncwarp();  // the buffer is rewritten by the next pass
           }
         }
       }
@@ -695,8 +829,8 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tmap_c,
                     const __grid_constant__ CUtensorMap tmap_al,
                     const __grid_constant__ CUtensorMap tmap_bl, float *__restrict__ C, int M,
-                    int N, int K, int64_t ldc, int c_tma, int group_m, int *watchdog,
-                    int mn3d, int stall, int snake) {
+                    int N, int K, int64_t ldc, int c_tma, int c_vec, int group_m,
+                    int *watchdog, int mn3d, int stall, int snake) {
   using G = Cfg2<KIND, AT, BT>;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -959,8 +1093,6 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
       t_prev = t_acc;
       const bool pace = t_span > 0 && tile + clusters < num_tiles;
       const int row0 = tm * G::BM + (int)rank * G::HM;  // this CTA's first row of C
-      const int row = row0 + quarter * 32 + lane;
-      float *crow = C + (int64_t)row * ldc;
       const uint32_t t_row =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * G::BN);
 #pragma unroll 1
@@ -973,26 +1105,33 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
         tmem_ld_32x32b_x32(t_row + (uint32_t)c0, r);
         tmem_wait_ld();
         const int col = tn * G::BN + c0;
-        if (c_tma && col + 32 <= N) {
-          // Each warp stages its 32 rows (row = lane) of the chunk in
-          // 128B-swizzled shared memory; the 128-row box goes out in one TMA
-          // store (full lines; rows past M are dropped by the hardware).  Only
-          // chunks wholly inside N go this way: at the inner edge a TMA store
-          // writes whole 16-byte granules, which would touch the ldc gap when N
-          // is not a multiple of 4.  The condition is the same in all four
-          // warps.  Two buffers; before one is refilled, the store issued from
-          // it two chunks ago must have read it.
-          const uint32_t buf = epi_base + (uint32_t)((epi_chunk & 1) * G::EPI_BUF_BYTES);
+        // Each warp stages its 32 rows (row = lane) of the chunk in
+        // 128B-swizzled shared memory.  A chunk wholly inside N of a C that
+        // TMA can write goes out as one 128-row box in one TMA store (full
+        // lines; rows past M are dropped by the hardware).  Other chunks (the
+        // inner edge, where a TMA store would write whole 16-byte granules
+        // and touch the ldc gap when N is not a multiple of 4, or a C that
+        // TMA cannot write) are written by the warp itself, row by row from
+        // its own 32 rows.  The conditions are the same in all four warps.
+        // With TMA stores: two buffers; before one is refilled, the store
+        // issued from it two chunks ago must have read it.  Without: buffer
+        // 0, which no TMA store reads.
+        const bool tma_chunk = c_tma && col + 32 <= N;
+        uint32_t buf = epi_base;
+        if (c_tma) {
+          buf = epi_base + (uint32_t)((epi_chunk & 1) * G::EPI_BUF_BYTES);
           if (issuer && epi_chunk >= 2) bulk_wait_group_read<1>();
           named_bar_sync<1, 32 * G::kEpiWarps>();
-          const uint32_t row_addr = buf + (uint32_t)(quarter * 32 * 128 + lane * 128);
+        }
+        const uint32_t wbuf = buf + (uint32_t)(quarter * 32 * 128);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t dst = row_addr + (uint32_t)(((c ^ (lane & 7)) << 4));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[4 * c]),
-                         "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
-                         : "memory");
-          }
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t dst = wbuf + (uint32_t)(lane * 128 + ((c ^ (lane & 7)) << 4));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[4 * c]),
+                       "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
+                       : "memory");
+        }
+        if (tma_chunk) {
           fence_proxy_async_smem();
           named_bar_sync<1, 32 * G::kEpiWarps>();
           if (issuer) {
@@ -1002,12 +1141,41 @@ __global__ void __launch_bounds__(Cfg2<KIND, AT, BT>::THREADS, 1)
             if (row0 < M) tma_store_2d(&tmap_c, buf, col, row0);
             bulk_commit_group();
           }
-          ++epi_chunk;
-        } else if (row < M) {
+        } else {
+          __syncwarp();
+          const int wrow0 = row0 + quarter * 32;  // C row of the warp's staged row 0
+          const float *wb = reinterpret_cast<const float *>(smem + (wbuf - base));
+          if (wrow0 < M && col < N) {
+            if (c_vec) {  // 16-byte stores: eight lanes to a row, four rows at a time
+              const int q = lane & 7, c4 = col + 4 * q;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (col + j < N) crow[col + j] = __uint_as_float(r[j]);
+              for (int i = 0; i < 8; ++i) {
+                const int rr = 4 * i + (lane >> 3);
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(wb + rr * 32 + ((q ^ (rr & 7)) << 2));
+                if (wrow0 + rr < M) {
+                  float *d = C + (int64_t)(wrow0 + rr) * ldc + c4;
+                  if (c4 + 4 <= N) {
+                    *reinterpret_cast<float4 *>(d) = v;
+                  } else {
+                    if (c4 < N) d[0] = v.x;
+                    if (c4 + 1 < N) d[1] = v.y;
+                    if (c4 + 2 < N) d[2] = v.z;
+                  }
+                }
+              }
+            } else {  // one element per lane, a row per instruction
+#pragma unroll 8
+              for (int rr = 0; rr < 32; ++rr) {
+                const float v = wb[rr * 32 + (((lane >> 2) ^ (rr & 7)) << 2) + (lane & 3)];
+                if (wrow0 + rr < M && col + lane < N) C[(int64_t)(wrow0 + rr) * ldc + col + lane] = v;
+              }
+            }
+          }
+          __syncwarp();  // the warp's rows are rewritten by the next chunk
+          if (c_tma && issuer) bulk_commit_group();  // one group per chunk
         }
+        if (c_tma) ++epi_chunk;
       }
       tc_fence_before();
       __syncwarp();
@@ -1298,7 +1466,7 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
   const int clusters = (int)(tiles < maxc ? tiles : maxc);
   e = launch_kernel(kern, dim3(2 * clusters), dim3(G::THREADS), G::SMEM_BYTES, stream, 2u, ta, tb,
-                    tc, tal, tbl, C, M, N, K, ldc, c_tma ? 1 : 0,
+                    tc, tal, tbl, C, M, N, K, ldc, c_tma ? 1 : 0, c_vec ? 1 : 0,
                     raster_group_m(G::ES == 4 ? 8 : 16), watchdog,
                     mn3d, test_stall(), snake_order(G::ES == 4));
   if (e == cudaSuccess) e = cudaGetLastError();
