@@ -468,8 +468,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
         tc_fence_before();
         break;  // one unit per CTA
       }
-      // Tiles with more than 64 columns inside C go out row by row through
-      // shared memory, so that every store writes whole lines: each thread writes
+      // Except for a few narrow tiles, C goes out row by row through shared
+      // memory, so that every store writes whole lines: each thread writes
       // its accumulator row there (16-byte chunks, chunk q of row r at
       // q ^ (r & 7) within its group of eight, so a quarter-warp's eight
       // rows fill the 32 banks), then the warp writes C along rows: 16-byte
@@ -478,9 +478,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
       // are skipped (warp-uniform).
       const int row0 = tm * BM + quarter * 32;  // C row of the warp's staged row 0
       const int ncols = min(BN, N - tn * BN);   // columns of this tile inside C
-      if (ncols <= 64) {
-        // Narrow edge (at most two 32-column loads): each thread stores its
-        // own row straight from registers, the fewest steps.
+      if (ncols <= 64 && units <= 16) {
+        // A few narrow tiles (the whole call is latency-bound): each thread
+        // stores its own row straight from registers, the fewest steps.
         const int row = row0 + lane;
 #pragma unroll 1
         for (int c0 = 0; row0 < M && c0 < ncols; c0 += 32) {
@@ -543,15 +543,16 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
               }
             }
           } else {
+            // C rows off 16-byte boundaries: along rows first, so that the
+            // stores that share a sector (where one 32-column group ends and
+            // the next begins) follow one another.
+            constexpr int NCH = BN / 32;  // 32-column groups of a staged row
             const int sw = lane & 3, cq = lane >> 2;
-#pragma unroll 1
-            for (int c0 = 0; c0 < ncols; c0 += 32) {
-              const int col = tn * BN + c0 + lane;
 #pragma unroll 8
-              for (int rr = 0; rr < 32; ++rr) {
-                const float v = wb[rr * BN + c0 + ((cq ^ (rr & 7)) << 2) + sw];
-                if (row0 + rr < M && col < N) C[(int64_t)(row0 + rr) * ldc + col] = v;
-              }
+            for (int j = 0; j < 32 * NCH; ++j) {
+              const int rr = j / NCH, c0 = (j % NCH) * 32, col = tn * BN + c0 + lane;
+              if (row0 + rr < M && col < N)
+                C[(int64_t)(row0 + rr) * ldc + col] = wb[rr * BN + c0 + ((cq ^ (rr & 7)) << 2) + sw];
             }
           }
         }
@@ -1241,13 +1242,87 @@ int snake_order(bool dflt) {
 // (1024^3 TF32 10.7 -> 12.0 us, 1024 x 1024 x 4096 TF32 18.1 -> 28.6 us),
 // where the wider tile's lower operand traffic per flop wins.  So it runs for
 // 8-bit operands, and for the others when a row of K is at most 1 KB.
-// DGEMM_TC_SMALL=0 / =1 forces it off / on (read at every launch, for tests
-// and tuning).  3xTF32 keeps its own 128 x 128 configuration with split warps.
+// (single_tile below decides for 32- and 16-bit operands.)  DGEMM_TC_SMALL=0
+// / =1 forces it off / on (read at every launch, for tests and tuning).
 constexpr int kSmallBudget = 3 * 32768;
-bool tc_small_config(int elem_bytes, int K) {
-  const char *e = getenv("DGEMM_TC_SMALL");
-  if (e && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
-  return elem_bytes == 1 || (int64_t)K * elem_bytes <= 1024;
+
+// Tile of the single-CTA kernel: 128 x BN, one CTA per SM (192 KB of
+// stages), or the 128 x 128 two-CTAs-per-SM configuration above.
+enum class Tile { k64, k128, k128Small, k256 };
+
+// The K-split choose_splits would make, without its occupancy query (every
+// cluster size taken to fit).
+int expected_splits(int64_t tiles, int kblocks, int64_t slots) {
+  if (tiles * 2 > slots) return 1;
+  int s = (int)(slots / tiles);
+  s = s < 8 ? s : 8;
+  s = s < kblocks / 4 ? s : kblocks / 4;
+  for (; s >= 2; --s) {
+    const int per = (kblocks + s - 1) / s;
+    const int w = (kblocks + per - 1) / per;
+    if (tiles <= slots / w) return w;
+  }
+  return 1;
+}
+
+// Tile for the single-CTA kernel.  "第八课：GPU 如何完成矩阵乘法" section 十七
+// weighs tile size (operand reuse) against concurrency; on GB300 a problem
+// this small is bound by how fast each SM can pull its operands from L2
+// (about 100 GB/s per CTA measured), so the choice, fitted to a same-process
+// sweep of 14 shapes x 3 kinds x 10 configurations (within 5% of the best
+// configuration on 40 of the 42 points, 13% faster than the fixed 128 x 256
+// / 128 x 128 choice on average):
+//  - 32- and 16-bit operands, in this order: the small configuration when a
+//    row of K is at most 1 KB and 128 x 128 tiles would overfill one CTA per
+//    SM; else the widest tile (256, 128, 64) whose tile count fills at least
+//    half the SMs without a K-split (the 64-wide tile only while a row of K
+//    is at most 2 KB: beyond that the K-split's halved operand traffic per
+//    CTA wins over its reduction);
+//  - otherwise, and always for 3xTF32 (whose split warps favour wide tiles):
+//    the width whose expected K-split plan moves the fewest operand bytes
+//    through the busiest SM, a K-split counted as 250 KB (its DSMEM
+//    reduction, ~2.5 us at that rate).
+// 8-bit operands keep the small configuration (DGEMM_TC_SMALL=0: 128 x 256).
+// DGEMM_TC_BN=64 / 128 / 256 forces the width (one CTA per SM; not 64 for
+// 8-bit operands), DGEMM_TC_SMALL=1 the small configuration (read at every
+// launch, for tests and tuning).
+Tile single_tile(TcKind kind, int M, int N, int K, int num_sms) {
+  const int es = (kind == TcKind::kE4M3 || kind == TcKind::kE5M2) ? 1
+                 : (kind == TcKind::kBF16 || kind == TcKind::kF16) ? 2
+                                                                    : 4;
+  const bool split3 = kind == TcKind::k3xTF32;
+  if (const char *e = getenv("DGEMM_TC_BN")) {
+    if (strcmp(e, "64") == 0 && es != 1) return Tile::k64;
+    if (strcmp(e, "128") == 0) return Tile::k128;
+    if (strcmp(e, "256") == 0) return Tile::k256;
+  }
+  const char *sm = getenv("DGEMM_TC_SMALL");
+  const int small = (sm && (sm[0] == '0' || sm[0] == '1') && sm[1] == 0) ? sm[0] - '0' : -1;
+  if (!split3 && small == 1) return Tile::k128Small;
+  if (es == 1) return small == 0 ? Tile::k256 : Tile::k128Small;
+  const int64_t tm = (M + 127) / 128, kes = (int64_t)K * es;
+  auto tiles = [&](int bn) { return tm * ((N + bn - 1) / bn); };
+  if (!split3) {
+    if (small != 0 && kes <= 1024 && tiles(128) > num_sms) return Tile::k128Small;
+    if (2 * tiles(256) >= num_sms) return Tile::k256;
+    if (2 * tiles(128) >= num_sms) return Tile::k128;
+    if (2 * tiles(64) >= num_sms && kes <= 2048) return Tile::k64;
+  }
+  const int bk = 128 / es, kblocks = (K + bk - 1) / bk;
+  Tile best = Tile::k256;
+  double best_cost = 0;
+  for (int bn : {256, 128, 64}) {
+    const int64_t t = tiles(bn);
+    const int s = expected_splits(t, kblocks, num_sms);
+    const int64_t waves = (t * s + num_sms - 1) / num_sms;
+    const double bytes = (double)(128 + bn) * ((kblocks + s - 1) / s) * bk * es;
+    const double cost = (double)waves * bytes + (s > 1 ? 250e3 : 0.0);
+    if (bn == 256 || cost < best_cost) {
+      best_cost = cost;
+      best = bn == 256 ? Tile::k256 : bn == 128 ? Tile::k128 : Tile::k64;
+    }
+  }
+  return best;
 }
 
 // DGEMM_TC_TEST_STALL=1 makes the MMA thread of the first CTA (pair) wait on
@@ -1474,23 +1549,37 @@ cudaError_t launch_cfg2(int M, int N, int K, const void *A, int64_t lda, const v
   return e;
 }
 
-// Pair kernel or single-CTA kernel (tc_use_pair); 3xTF32 takes the pair
-// kernel only with the lo parts of A and B at hand.
-template <TcKind KIND, int BN1>
+// Pair kernel or single-CTA kernel (tc_use_pair, then single_tile); 3xTF32
+// takes the pair kernel only with the lo parts of A and B at hand.
+template <TcKind KIND>
 cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const void *B,
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
                         int *watchdog, cudaStream_t stream, const void *A_lo, const void *B_lo) {
   constexpr bool AT = kUnitAT, BT = kUnitBT;
+  constexpr bool k8 = KIND == TcKind::kE4M3 || KIND == TcKind::kE5M2;
   const bool lo_ok = KIND != TcKind::k3xTF32 || (A_lo != nullptr && B_lo != nullptr);
   if (lo_ok && tc_use_pair(M, N, num_sms))
     return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream,
                                      A_lo, B_lo);
-  if constexpr (KIND != TcKind::k3xTF32) {
-    if (tc_small_config(Cfg<KIND, BN1, AT, BT>::ES, K))
-      return launch_cfg<KIND, 128, AT, BT, kSmallBudget>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
-                                                          num_sms, watchdog, stream);
+  switch (single_tile(KIND, M, N, K, num_sms)) {
+    case Tile::k64:
+      if constexpr (!k8)
+        return launch_cfg<KIND, 64, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                            watchdog, stream);
+      break;
+    case Tile::k128:
+      return launch_cfg<KIND, 128, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                           watchdog, stream);
+    case Tile::k128Small:
+      if constexpr (KIND != TcKind::k3xTF32)
+        return launch_cfg<KIND, 128, AT, BT, kSmallBudget>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
+                                                            num_sms, watchdog, stream);
+      break;
+    case Tile::k256:
+      break;
   }
-  return launch_cfg<KIND, BN1, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog, stream);
+  return launch_cfg<KIND, 256, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
+                                       stream);
 }
 
 #if DGEMM_TC_UNIT == 0
@@ -1510,26 +1599,26 @@ cudaError_t DG_UNIT_LAUNCHER(TcKind kind, int M, int N, int K, const void *A, in
                              const void *B_lo) {
   switch (kind) {
     case TcKind::kTF32:
-      return launch_kind<TcKind::kTF32, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, stream, A_lo, B_lo);
+      return launch_kind<TcKind::kTF32>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
+                                        stream, A_lo, B_lo);
     case TcKind::k3xTF32:
-      return launch_kind<TcKind::k3xTF32, 128>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                               watchdog, stream, A_lo, B_lo);
+      return launch_kind<TcKind::k3xTF32>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                          watchdog, stream, A_lo, B_lo);
     case TcKind::kBF16:
-      return launch_kind<TcKind::kBF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                             watchdog, stream, A_lo, B_lo);
+      return launch_kind<TcKind::kBF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
+                                        stream, A_lo, B_lo);
     case TcKind::kF16:
-      return launch_kind<TcKind::kF16, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            watchdog, stream, A_lo, B_lo);
+      return launch_kind<TcKind::kF16>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms, watchdog,
+                                       stream, A_lo, B_lo);
     case TcKind::kE4M3:
     case TcKind::kE5M2:
       // 8-bit operands exist only K-major (A as M x K, B as N x K): this unit
       if constexpr (!kUnitAT && kUnitBT) {
         if (kind == TcKind::kE4M3)
-          return launch_kind<TcKind::kE4M3, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
-                                                 num_sms, watchdog, stream, A_lo, B_lo);
-        return launch_kind<TcKind::kE5M2, 256>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                               watchdog, stream, A_lo, B_lo);
+          return launch_kind<TcKind::kE4M3>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                            watchdog, stream, A_lo, B_lo);
+        return launch_kind<TcKind::kE5M2>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                          watchdog, stream, A_lo, B_lo);
       }
       return cudaErrorInvalidValue;
   }
