@@ -225,25 +225,25 @@ _NCU = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_dura
 _WHERE = "one GB300 of the pool, 2026-12-02, after the same command exited 0 without ncu"
 RECORDED_TRAFFIC = {
     ("tf32", "square-8192 fp32"): {
-        "bytes": 2050968576 + 258755328, "sha": "e3ec734d5641", "kernel": "tc2_gemm_kernel<TF32>",
-        "read": 2050968576, "write": 258755328, "command": _NCU.format(k="tc2_gemm", m="tf32"),
+        "bytes": 2142034176 + 259039744, "sha": "039b7e13ff04", "kernel": "tc2_gemm_kernel<TF32>",
+        "read": 2142034176, "write": 259039744, "command": _NCU.format(k="tc2_gemm", m="tf32"),
         "where": _WHERE},
     ("3xtf32", "square-8192 fp32"): {
-        "bytes": 4318036480 + 262111488, "sha": "e3ec734d5641",
-        "kernel": "tc2_gemm_kernel<3xTF32> (lo parts loaded too)", "read": 4318036480,
-        "write": 262111488, "command": _NCU.format(k="tc2_gemm", m="3xtf32"), "where": _WHERE},
+        "bytes": 4320936960 + 262190080, "sha": "039b7e13ff04",
+        "kernel": "tc2_gemm_kernel<3xTF32> (lo parts loaded too)", "read": 4320936960,
+        "write": 262190080, "command": _NCU.format(k="tc2_gemm", m="3xtf32"), "where": _WHERE},
     ("bf16", "transformer-layer 16384x14336x4096 bf16"): {
-        "bytes": 1024661248 + 907866368, "sha": "e3ec734d5641", "kernel": "tc2_gemm_kernel<BF16>",
-        "read": 1024661248, "write": 907866368, "command": _NCU.format(k="tc2_gemm", m="bf16"),
+        "bytes": 1034631936 + 910214656, "sha": "039b7e13ff04", "kernel": "tc2_gemm_kernel<BF16>",
+        "read": 1034631936, "write": 910214656, "command": _NCU.format(k="tc2_gemm", m="bf16"),
         "where": _WHERE},
     ("e4m3", "transformer-layer 16384x14336x4096 e4m3"): {
-        "bytes": 311126272 + 888528640, "sha": "e3ec734d5641",
+        "bytes": 317118464 + 889402624, "sha": "039b7e13ff04",
         "kernel": "tc2_gemm_kernel<E4M3> (B stored N x K after the transpose launch)",
-        "read": 311126272, "write": 888528640, "command": _NCU.format(k="tc2_gemm", m="e4m3"),
+        "read": 317118464, "write": 889402624, "command": _NCU.format(k="tc2_gemm", m="e4m3"),
         "where": _WHERE},
     ("simt", "square-8192 fp32"): {
-        "bytes": 2855109632 + 262675456, "sha": "a022c02811ef", "kernel": "sgemm_ring_kernel",
-        "read": 2855109632, "write": 262675456, "command": _NCU.format(k="sgemm_ring", m="simt"),
+        "bytes": 2853677056 + 262401024, "sha": "c1a7e011dcd8", "kernel": "sgemm_ring_kernel",
+        "read": 2853677056, "write": 262401024, "command": _NCU.format(k="sgemm_ring", m="simt"),
         "where": _WHERE},
 }
 
