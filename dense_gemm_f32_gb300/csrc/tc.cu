@@ -156,7 +156,7 @@ struct Cfg {
   static constexpr int PART_PITCH = BN + 4;
   static constexpr int MAX_SPLITS = 8;  // portable cluster size
 
-  static_assert(BN % BOX == 0 && BM % BOX == 0, "whole number of MN-major boxes");
+  static_assert((!AT || BM % BOX == 0) && (BT || BN % BOX == 0), "whole number of MN-major boxes");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
@@ -1234,16 +1234,9 @@ int snake_order(bool dflt) {
 // 3 stages (96 KB of stages, 256 TMEM columns), so that two CTAs fit on an
 // SM: the next call's CTAs can then start their set-up beside the previous
 // call's (programmatic dependent launch), and each CTA writes half the C of a
-// 128 x 256 tile.  Measured on GB300 (graph replay, same process, against the
-// 128 x 256 4-stage configuration): ahead for 8-bit operands at every small
-// shape tried (1024^3 E4M3 12.5 -> 9.4 us, 2048 x 1024 x 1024 12.8 -> 8.9 us)
-// and for every kind when K is short (64^3 TF32 3.9 -> 3.2 us, 1024 x 1024 x
-// 256 TF32 10.3 -> 8.3 us); behind for 32- and 16-bit operands with longer K
-// (1024^3 TF32 10.7 -> 12.0 us, 1024 x 1024 x 4096 TF32 18.1 -> 28.6 us),
-// where the wider tile's lower operand traffic per flop wins.  So it runs for
-// 8-bit operands, and for the others when a row of K is at most 1 KB.
-// (single_tile below decides for 32- and 16-bit operands.)  DGEMM_TC_SMALL=0
-// / =1 forces it off / on (read at every launch, for tests and tuning).
+// 128 x 256 tile.  It pays where 128 x 128 tiles would overfill one CTA per
+// SM and a row of K is short (2048^2 x 256 TF32: 8.3 us against 10.0 at one
+// CTA per SM); single_tile below decides.
 constexpr int kSmallBudget = 3 * 32768;
 
 // Tile of the single-CTA kernel: 128 x BN, one CTA per SM (192 KB of
@@ -1271,8 +1264,9 @@ int expected_splits(int64_t tiles, int kblocks, int64_t slots) {
 // (about 100 GB/s per CTA measured), so the choice, fitted to a same-process
 // sweep of 14 shapes x 3 kinds x 10 configurations (within 5% of the best
 // configuration on 40 of the 42 points, 13% faster than the fixed 128 x 256
-// / 128 x 128 choice on average):
-//  - 32- and 16-bit operands, in this order: the small configuration when a
+// / 128 x 128 choice on average) and checked on the same shapes for 8-bit
+// operands (within 5% on 13 of 14):
+//  - every kind but 3xTF32, in this order: the small configuration when a
 //    row of K is at most 1 KB and 128 x 128 tiles would overfill one CTA per
 //    SM; else the widest tile (256, 128, 64) whose tile count fills at least
 //    half the SMs without a K-split (the 64-wide tile only while a row of K
@@ -1282,24 +1276,22 @@ int expected_splits(int64_t tiles, int kblocks, int64_t slots) {
 //    the width whose expected K-split plan moves the fewest operand bytes
 //    through the busiest SM, a K-split counted as 250 KB (its DSMEM
 //    reduction, ~2.5 us at that rate).
-// 8-bit operands keep the small configuration (DGEMM_TC_SMALL=0: 128 x 256).
-// DGEMM_TC_BN=64 / 128 / 256 forces the width (one CTA per SM; not 64 for
-// 8-bit operands), DGEMM_TC_SMALL=1 the small configuration (read at every
-// launch, for tests and tuning).
+// DGEMM_TC_BN=64 / 128 / 256 forces the width (one CTA per SM),
+// DGEMM_TC_SMALL=1 / =0 forces the small configuration / rules it out (read
+// at every launch, for tests and tuning).
 Tile single_tile(TcKind kind, int M, int N, int K, int num_sms) {
   const int es = (kind == TcKind::kE4M3 || kind == TcKind::kE5M2) ? 1
                  : (kind == TcKind::kBF16 || kind == TcKind::kF16) ? 2
                                                                     : 4;
   const bool split3 = kind == TcKind::k3xTF32;
   if (const char *e = getenv("DGEMM_TC_BN")) {
-    if (strcmp(e, "64") == 0 && es != 1) return Tile::k64;
+    if (strcmp(e, "64") == 0) return Tile::k64;
     if (strcmp(e, "128") == 0) return Tile::k128;
     if (strcmp(e, "256") == 0) return Tile::k256;
   }
   const char *sm = getenv("DGEMM_TC_SMALL");
   const int small = (sm && (sm[0] == '0' || sm[0] == '1') && sm[1] == 0) ? sm[0] - '0' : -1;
   if (!split3 && small == 1) return Tile::k128Small;
-  if (es == 1) return small == 0 ? Tile::k256 : Tile::k128Small;
   const int64_t tm = (M + 127) / 128, kes = (int64_t)K * es;
   auto tiles = [&](int bn) { return tm * ((N + bn - 1) / bn); };
   if (!split3) {
@@ -1563,10 +1555,8 @@ cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const v
                                      A_lo, B_lo);
   switch (single_tile(KIND, M, N, K, num_sms)) {
     case Tile::k64:
-      if constexpr (!k8)
-        return launch_cfg<KIND, 64, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
-                                            watchdog, stream);
-      break;
+      return launch_cfg<KIND, 64, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
+                                          watchdog, stream);
     case Tile::k128:
       return launch_cfg<KIND, 128, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                            watchdog, stream);

@@ -3,7 +3,8 @@
 Below the CTA-pair threshold the library picks a 128 x BN tile (BN = 64, 128
 or 256 with one CTA per SM, or the 128 x 128 two-CTAs-per-SM configuration)
 by problem shape; DGEMM_TC_BN=64 / 128 / 256 forces a width.  Every width in
-every mode against the CPU oracle, through ragged and unaligned operands,
+every tensor-core mode (8-bit operands read K-major, B transposed first)
+against the CPU oracle, through ragged and unaligned operands,
 the K-split and guarded C; without the K-split all widths give the same bits
 (each output element sees the same multiply-adds in the same order); and the
 default choice on a few shapes whose best width is known.
@@ -19,7 +20,7 @@ import dense_gemm_f32_gb300 as dg
 pytestmark = pytest.mark.gpu
 
 WIDTHS = ("64", "128", "256")
-MODES = ("tf32", "3xtf32", "bf16", "fp16")
+MODES = ("tf32", "3xtf32", "bf16", "fp16", "e4m3", "e5m2")
 SHAPES = [(1, 1, 1), (64, 64, 64), (130, 200, 70), (1000, 1013, 997), (512, 384, 4096),
           (1024, 1024, 256)]
 
@@ -63,7 +64,7 @@ def test_widths_agree_bit_for_bit_without_split(mode, monkeypatch):
         assert torch.equal(out["64"], out["128"]) and torch.equal(out["64"], out["256"]), mode
 
 
-@pytest.mark.parametrize("mode", ("tf32", "bf16"))
+@pytest.mark.parametrize("mode", ("tf32", "bf16", "e4m3"))
 @pytest.mark.parametrize("bn", WIDTHS)
 @pytest.mark.parametrize("split", ["0", "4"])
 def test_widths_guard_bands_unaligned_operands_and_ldc(mode, bn, split, monkeypatch):
