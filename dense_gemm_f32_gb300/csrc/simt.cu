@@ -827,7 +827,7 @@ cudaError_t launch_simt_cfg(int M, int N, int K, const float *A, int64_t lda, co
 // a barrier that nothing arrives at: the wait runs out after ~2 s and the
 // kernel takes its abort path (watchdog site code, drained copies,
 // incomplete C).  For the failure-detection test only; read at every launch.
-int simt_test_stall() {
+[[maybe_unused]] int simt_test_stall() {
   const char *e = getenv("DGEMM_SIMT_TEST_STALL");
   return (e && e[0] == '1') ? 1 : 0;
 }

@@ -1548,7 +1548,6 @@ cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const v
                         int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
                         int *watchdog, cudaStream_t stream, const void *A_lo, const void *B_lo) {
   constexpr bool AT = kUnitAT, BT = kUnitBT;
-  constexpr bool k8 = KIND == TcKind::kE4M3 || KIND == TcKind::kE5M2;
   const bool lo_ok = KIND != TcKind::k3xTF32 || (A_lo != nullptr && B_lo != nullptr);
   if (lo_ok && tc_use_pair(M, N, num_sms))
     return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream,
