@@ -108,3 +108,23 @@ def test_default_choice_matches_the_oracle(mode, monkeypatch):
         rows = np.arange(0, M, 37)
         ref, S = gu.oracle_rows(A, B, rows)
         gu.assert_close(C[rows], ref, S, gu.TOL[mode], f"{mode} default {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("mode", ("tf32", "bf16", "e4m3"))
+@pytest.mark.parametrize("bn", WIDTHS)
+def test_persistent_ctas_guard_bands_and_unaligned_ldc(mode, bn, monkeypatch):
+    """More tiles than CTA slots: persistent CTAs, whose epilogue stages C
+    through a small per-warp buffer while the next tile's operands arrive;
+    with an ldc that breaks 16-byte rows, sentinels around and between the
+    rows of C, and a ragged last tile row and column."""
+    monkeypatch.setenv("DGEMM_TC_PAIR", "0")
+    monkeypatch.setenv("DGEMM_TC_BN", bn)
+    monkeypatch.setenv("DGEMM_TC_SPLITK", "0")
+    M, N, K, ldc = 4001, 1030, 200, 1033
+    A, B = inputs.make_random(M, N, K, seed=29, dist="normal", dtype=gu.in_dtype(mode))
+    buf, view = gu.guarded_output(M, N, ldc)
+    gu.run(mode, A.cuda(), B.cuda(), out=view)
+    gu.assert_guards_intact(buf, M, N, ldc)
+    rows = np.concatenate([np.arange(0, M, 61), [M - 1]])
+    ref, S = gu.oracle_rows(A, B, rows)
+    gu.assert_close(view.cpu().numpy()[rows], ref, S, gu.TOL[mode], f"{mode} BN={bn} persistent")
