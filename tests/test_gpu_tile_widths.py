@@ -128,3 +128,25 @@ def test_persistent_ctas_guard_bands_and_unaligned_ldc(mode, bn, monkeypatch):
     rows = np.concatenate([np.arange(0, M, 61), [M - 1]])
     ref, S = gu.oracle_rows(A, B, rows)
     gu.assert_close(view.cpu().numpy()[rows], ref, S, gu.TOL[mode], f"{mode} BN={bn} persistent")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("bn", WIDTHS)
+@pytest.mark.parametrize("ta, tb", [(False, True), (True, False), (True, True)])
+def test_every_width_transposed_operands(ta, tb, bn, mode, monkeypatch):
+    """op(A) = A^T and / or op(B) = B^T (the MMA reads such operands MN- or
+    K-major as stored; 8-bit ones are transposed into K-major form first) at
+    every width, ragged sizes, with and without the K-split."""
+    monkeypatch.setenv("DGEMM_TC_PAIR", "0")
+    monkeypatch.setenv("DGEMM_TC_BN", bn)
+    for (M, N, K, split) in [(300, 259, 301, "0"), (257, 385, 1030, "4")]:
+        monkeypatch.setenv("DGEMM_TC_SPLITK", split)
+        A, B = inputs.make_random(M, N, K, seed=M + N + K + ta + 2 * tb, dist="normal",
+                                  dtype=gu.in_dtype(mode))
+        Ad = (A.t().contiguous() if ta else A).cuda()
+        Bd = (B.t().contiguous() if tb else B).cuda()
+        C = dg.matmul(Ad, Bd, mode=mode, trans_a=ta, trans_b=tb)
+        torch.cuda.synchronize()
+        ref, S = gu.oracle_full(A, B)
+        gu.assert_close(C.cpu().numpy(), ref, S, gu.TOL[mode],
+                        f"{mode} BN={bn} ta={ta} tb={tb} {M}x{N}x{K} split={split}")
