@@ -96,7 +96,8 @@ enum : int {
 // AT: A is stored K x M (op(A) = A^T), read MN-major.  BT: B is stored N x K
 // (op(B) = B^T), read K-major.  The defaults are the row-major A (K-major)
 // and B (MN-major) of the plain product.
-template <TcKind KIND, int BN_, bool AT_ = false, bool BT_ = false, int BUDGET_ = 196608>
+template <TcKind KIND, int BN_, bool AT_ = false, bool BT_ = false, int BUDGET_ = 196608,
+          int KD_ = 1>
 struct Cfg {
   static constexpr bool AT = AT_, BT = BT_;
   // 16-bit operands (BF16 or FP16, tcgen05 kind::f16) vs 32-bit (TF32 kinds)
@@ -113,19 +114,23 @@ struct Cfg {
   static constexpr bool kSplit = KIND == TcKind::k3xTF32;
   static constexpr int BN = BN_;
   static constexpr int ES = k8 ? 1 : k16 ? 2 : 4;  // operand element bytes
-  static constexpr int BK = 128 / ES;             // k per stage: one 128-B swizzle row
+  // k per stage: KD 128-byte swizzle rows (a TMA load costs a nearly fixed
+  // time per box on this part, so deeper stages move more bytes per second)
+  static constexpr int KD = KD_;
+  static constexpr int BK = KD * 128 / ES;
   static constexpr int UMMA_K = 32 / ES;          // k per MMA instruction (32 bytes)
   static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per stage (per product)
   static constexpr int BOX = 128 / ES;            // elements in one 128-byte swizzle row
   static constexpr int BOX_N = BOX;               // N columns per MN-major B box
-  static constexpr int A_BYTES = BM * 128;        // 128 M x BK, either major
-  static constexpr int B_BYTES = BN * 128;        // BN N x BK, either major
+  static constexpr int A_BYTES = BM * 128 * KD;   // 128 M x BK, either major
+  static constexpr int B_BYTES = BN * 128 * KD;   // BN N x BK, either major
   // MN-major operands arrive as boxes of 128 bytes (of M or N) x BK rows;
-  // K-major operands as one box of BK x (rows).
-  static constexpr int A_BOXES = AT ? BM / BOX : 1;
-  static constexpr int A_BOX_BYTES = AT ? BK * 128 : A_BYTES;
-  static constexpr int B_BOXES = BT ? 1 : BN / BOX;
-  static constexpr int B_BOX_BYTES = BT ? B_BYTES : BK * 128;
+  // K-major operands as KD boxes of 128 bytes of K x (rows), one after the
+  // other (the box stride then is one such box).
+  static constexpr int A_BOXES = AT ? BM / BOX : KD;
+  static constexpr int A_BOX_BYTES = AT ? BK * 128 : BM * 128;
+  static constexpr int B_BOXES = BT ? KD : BN / BOX;
+  static constexpr int B_BOX_BYTES = BT ? BN * 128 : BK * 128;
   static constexpr int RAW_BYTES = A_BYTES + B_BYTES;               // what TMA writes
   static constexpr int STAGE_BYTES = RAW_BYTES * (kSplit ? 2 : 1);  // + lo copies
   // stages that fit the shared-memory budget: 192 KB (one CTA per SM), or
@@ -157,6 +162,8 @@ struct Cfg {
   static constexpr int MAX_SPLITS = 8;  // portable cluster size
 
   static_assert((!AT || BM % BOX == 0) && (BT || BN % BOX == 0), "whole number of MN-major boxes");
+  static_assert(KD == 1 || KD == 2, "one or two swizzle rows of K per stage");
+  static_assert(BK <= 256, "an MN-major box holds at most 256 rows of K");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(ACC_COLS <= 512, "TMEM has 512 columns");
@@ -206,8 +213,8 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t saddr, int k, uint32_t
   if constexpr (kMN)
     return smem_desc(saddr + (uint32_t)(k * (G::UMMA_K / 8) * 1024), box_bytes, G::MN_SBO,
                      G::MN_LAYOUT);
-  else
-    return smem_desc(saddr + (uint32_t)(k * 32), 16, 1024);
+  else  // K-major: 4 MMAs of 32 bytes of K per 128-byte box, boxes box_bytes apart
+    return smem_desc(saddr + (uint32_t)((k >> 2) * box_bytes + (k & 3) * 32), 16, 1024);
 }
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
@@ -226,13 +233,13 @@ __device__ __forceinline__ void watchdog_trip(int *watchdog, int site, volatile 
   *abort_flag = 1;
 }
 
-template <TcKind KIND, int BN, bool AT, bool BT, int BUDGET>
-__global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
+template <TcKind KIND, int BN, bool AT, bool BT, int BUDGET, int KD>
+__global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET, KD>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, float *__restrict__ C, int M,
                    int N, int K, int64_t ldc, int c_vec, int group_m, int *watchdog,
                    int splits, int mn3d, int stall) {
-  using G = Cfg<KIND, BN, AT, BT, BUDGET>;
+  using G = Cfg<KIND, BN, AT, BT, BUDGET, KD>;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms.
@@ -326,8 +333,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
               if constexpr (AT)  // A stored K x M: boxes of BOX columns of M x BK rows
                 tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage),
                             tm * BM + j * G::BOX, kb * G::BK);
-              else
-                tma_load_2d(a_tile(stage), &tmap_a, full_bar(stage), kb * G::BK, tm * BM);
+              else  // A stored M x K: box j holds k-chunk j (BOX of K) x BM rows
+                tma_load_2d(a_tile(stage) + j * G::A_BOX_BYTES, &tmap_a, full_bar(stage),
+                            kb * G::BK + j * G::BOX, tm * BM);
             }
           }
           if (!BT && (mn3d & kB3d)) {  // B stored K x N, all its column blocks at once
@@ -335,8 +343,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, AT, BT, BUDGET>::THREADS, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < G::B_BOXES; ++j) {
-              if constexpr (BT)  // B stored N x K: one box of BK x BN
-                tma_load_2d(b_tile(stage), &tmap_b, full_bar(stage), kb * G::BK, tn * BN);
+              if constexpr (BT)  // B stored N x K: box j holds k-chunk j x BN rows
+                tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
+                            kb * G::BK + j * G::BOX, tn * BN);
               else
                 tma_load_2d(b_tile(stage) + j * G::B_BOX_BYTES, &tmap_b, full_bar(stage),
                             tn * BN + j * G::BOX_N, kb * G::BK);
@@ -1240,8 +1249,9 @@ int snake_order(bool dflt) {
 constexpr int kSmallBudget = 3 * 32768;
 
 // Tile of the single-CTA kernel: 128 x BN, one CTA per SM (192 KB of
-// stages), or the 128 x 128 two-CTAs-per-SM configuration above.
-enum class Tile { k64, k128, k128Small, k256 };
+// stages), or the 128 x 128 two-CTAs-per-SM configuration above; "Deep":
+// stages two 128-byte swizzle rows of K deep.
+enum class Tile { k64, k64Deep, k128, k128Deep, k128Small, k256 };
 
 // The K-split choose_splits would make, without its occupancy query (every
 // cluster size taken to fit).
@@ -1270,37 +1280,61 @@ int expected_splits(int64_t tiles, int kblocks, int64_t slots) {
 //    row of K is at most 1 KB and 128 x 128 tiles would overfill one CTA per
 //    SM; else the widest tile (256, 128, 64) whose tile count fills at least
 //    half the SMs without a K-split (the 64-wide tile only while a row of K
-//    is at most 2 KB: beyond that the K-split's halved operand traffic per
+//    is at most 4 KB: beyond that the K-split's halved operand traffic per
 //    CTA wins over its reduction);
 //  - otherwise, and always for 3xTF32 (whose split warps favour wide tiles):
 //    the width whose expected K-split plan moves the fewest operand bytes
 //    through the busiest SM, a K-split counted as 250 KB (its DSMEM
-//    reduction, ~2.5 us at that rate).
+//    reduction, ~2.5 us at that rate);
+//  - 128 x 64 and 128 x 128 tiles then take stages two swizzle rows of K
+//    deep (48 and 64 KB), when K fills at least four shallow stages and
+//    unless that lowers the K-split's part count: a TMA
+//    load costs a nearly fixed time per box, so a deep stage fills about
+//    twice as fast (measured: 1024^3 TF32 10.6 -> 9.6 us, BF16 1536^3
+//    10.9 -> 9.3 us).
 // DGEMM_TC_BN=64 / 128 / 256 forces the width (one CTA per SM),
-// DGEMM_TC_SMALL=1 / =0 forces the small configuration / rules it out (read
-// at every launch, for tests and tuning).
+// DGEMM_TC_KD=1 / 2 the stage depth (2: wherever it fits), DGEMM_TC_SMALL=1
+// / =0 forces the small configuration / rules it out (read at every launch,
+// for tests and tuning).
 Tile single_tile(TcKind kind, int M, int N, int K, int num_sms) {
   const int es = (kind == TcKind::kE4M3 || kind == TcKind::kE5M2) ? 1
                  : (kind == TcKind::kBF16 || kind == TcKind::kF16) ? 2
                                                                     : 4;
   const bool split3 = kind == TcKind::k3xTF32;
+  const char *kde = getenv("DGEMM_TC_KD");
+  const int kd_env = (kde && (kde[0] == '1' || kde[0] == '2') && kde[1] == 0) ? kde[0] - '0' : 0;
+  // 128 x 64 and 128 x 128 tiles take deep stages unless that halves the
+  // k-blocks a K-split would share out (3xTF32: 128 x 64 only, its deep
+  // 128 x 128 stages would not fit twice)
+  const int bk = 128 / es, kblocks = (K + bk - 1) / bk;
+  const int64_t tm = (M + 127) / 128, kes = (int64_t)K * es;
+  auto tiles = [&](int bn) { return tm * ((N + bn - 1) / bn); };
+  auto deepen = [&](Tile t) {
+    if (kd_env == 1) return t;
+    const bool can = t == Tile::k64 || (t == Tile::k128 && !split3);
+    // (K of at most three shallow stages: a deep stage would be half empty)
+    if (!can || (kd_env != 2 && kblocks < 4)) return t;
+    const int64_t n = tiles(t == Tile::k64 ? 64 : 128);
+    if (kd_env != 2 && expected_splits(n, (kblocks + 1) / 2, num_sms) !=
+                           expected_splits(n, kblocks, num_sms))
+      return t;
+    return t == Tile::k64 ? Tile::k64Deep : Tile::k128Deep;
+  };
   if (const char *e = getenv("DGEMM_TC_BN")) {
-    if (strcmp(e, "64") == 0) return Tile::k64;
-    if (strcmp(e, "128") == 0) return Tile::k128;
+    if (strcmp(e, "64") == 0) return kd_env == 2 ? deepen(Tile::k64) : Tile::k64;
+    if (strcmp(e, "128") == 0) return kd_env == 2 ? deepen(Tile::k128) : Tile::k128;
     if (strcmp(e, "256") == 0) return Tile::k256;
   }
   const char *sm = getenv("DGEMM_TC_SMALL");
   const int small = (sm && (sm[0] == '0' || sm[0] == '1') && sm[1] == 0) ? sm[0] - '0' : -1;
   if (!split3 && small == 1) return Tile::k128Small;
-  const int64_t tm = (M + 127) / 128, kes = (int64_t)K * es;
-  auto tiles = [&](int bn) { return tm * ((N + bn - 1) / bn); };
   if (!split3) {
     if (small != 0 && kes <= 1024 && tiles(128) > num_sms) return Tile::k128Small;
     if (2 * tiles(256) >= num_sms) return Tile::k256;
-    if (2 * tiles(128) >= num_sms) return Tile::k128;
-    if (2 * tiles(64) >= num_sms && kes <= 2048) return Tile::k64;
+    if (2 * tiles(128) >= num_sms) return deepen(Tile::k128);
+    if (2 * tiles(64) >= num_sms && kes <= (kd_env == 1 ? 2048 : 4096))
+      return deepen(Tile::k64);
   }
-  const int bk = 128 / es, kblocks = (K + bk - 1) / bk;
   Tile best = Tile::k256;
   double best_cost = 0;
   for (int bn : {256, 128, 64}) {
@@ -1314,7 +1348,7 @@ Tile single_tile(TcKind kind, int M, int N, int K, int num_sms) {
       best = bn == 256 ? Tile::k256 : bn == 128 ? Tile::k128 : Tile::k64;
     }
   }
-  return best;
+  return deepen(best);
 }
 
 // DGEMM_TC_TEST_STALL=1 makes the MMA thread of the first CTA (pair) wait on
@@ -1372,13 +1406,13 @@ bool make_operand_maps(CUtensorMap *ta, CUtensorMap *tb, int M, int N, int K, co
     ok_a = true;
   } else {
     ok_a = G::AT ? make_map(ta, A, dt, G::ES, K, M, lda, G::BOX, G::BK, mn_swz)
-                 : make_map(ta, A, dt, G::ES, M, K, lda, G::BK, rows_a, CU_TENSOR_MAP_SWIZZLE_128B);
+                 : make_map(ta, A, dt, G::ES, M, K, lda, G::BOX, rows_a, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!G::BT && make_map3(tb, B, dt, G::ES, K, N, ldb, G::BOX, G::BK, cols_b / G::BOX, mn_swz)) {
     *mn3d |= kB3d;
     ok_b = true;
   } else {
-    ok_b = G::BT ? make_map(tb, B, dt, G::ES, N, K, ldb, G::BK, cols_b, CU_TENSOR_MAP_SWIZZLE_128B)
+    ok_b = G::BT ? make_map(tb, B, dt, G::ES, N, K, ldb, G::BOX, cols_b, CU_TENSOR_MAP_SWIZZLE_128B)
                  : make_map(tb, B, dt, G::ES, K, N, ldb, G::BOX, G::BK, mn_swz);
   }
   return ok_a && ok_b;
@@ -1443,16 +1477,16 @@ int choose_splits(Kern kern, int threads, int smem, int dev, int64_t tiles, int 
   return 1;
 }
 
-template <TcKind KIND, int BN, bool AT, bool BT, int BUDGET = 196608>
+template <TcKind KIND, int BN, bool AT, bool BT, int BUDGET = 196608, int KD = 1>
 cudaError_t launch_cfg(int M, int N, int K, const void *A, int64_t lda, const void *B,
                        int64_t ldb, float *C, int64_t ldc, bool c_vec, int num_sms,
                        int *watchdog, cudaStream_t stream) {
-  using G = Cfg<KIND, BN, AT, BT, BUDGET>;
+  using G = Cfg<KIND, BN, AT, BT, BUDGET, KD>;
   CUtensorMap ta, tb;
   int mn3d = 0;
   if (!make_operand_maps<G, KIND>(&ta, &tb, M, N, K, A, lda, B, ldb, BM, BN, &mn3d))
     return cudaErrorInvalidValue;
-  auto kern = tc_gemm_kernel<KIND, BN, AT, BT, BUDGET>;
+  auto kern = tc_gemm_kernel<KIND, BN, AT, BT, BUDGET, KD>;
   static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1553,9 +1587,17 @@ cudaError_t launch_kind(int M, int N, int K, const void *A, int64_t lda, const v
     return launch_cfg2<KIND, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, watchdog, stream,
                                      A_lo, B_lo);
   switch (single_tile(KIND, M, N, K, num_sms)) {
+    case Tile::k64Deep:
+      return launch_cfg<KIND, 64, AT, BT, 196608, 2>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
+                                                      num_sms, watchdog, stream);
     case Tile::k64:
       return launch_cfg<KIND, 64, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                           watchdog, stream);
+    case Tile::k128Deep:  // (never chosen for 3xTF32)
+      if constexpr (KIND != TcKind::k3xTF32)
+        return launch_cfg<KIND, 128, AT, BT, 196608, 2>(M, N, K, A, lda, B, ldb, C, ldc, c_vec,
+                                                         num_sms, watchdog, stream);
+      [[fallthrough]];
     case Tile::k128:
       return launch_cfg<KIND, 128, AT, BT>(M, N, K, A, lda, B, ldb, C, ldc, c_vec, num_sms,
                                            watchdog, stream);
