@@ -225,25 +225,25 @@ _NCU = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_dura
 _WHERE = "one GB300 of the pool, 2026-12-02, after the same command exited 0 without ncu"
 RECORDED_TRAFFIC = {
     ("tf32", "square-8192 fp32"): {
-        "bytes": 2060247040 + 258928640, "sha": "4f1544a5bd16", "kernel": "tc2_gemm_kernel<TF32>",
-        "read": 2060247040, "write": 258928640, "command": _NCU.format(k="tc2_gemm", m="tf32"),
+        "bytes": 2044077312 + 259028480, "sha": "8caeb4a95d22", "kernel": "tc2_gemm_kernel<TF32>",
+        "read": 2044077312, "write": 259028480, "command": _NCU.format(k="tc2_gemm", m="tf32"),
         "where": _WHERE},
     ("3xtf32", "square-8192 fp32"): {
-        "bytes": 4323323392 + 262121984, "sha": "4f1544a5bd16",
-        "kernel": "tc2_gemm_kernel<3xTF32> (lo parts loaded too)", "read": 4323323392,
-        "write": 262121984, "command": _NCU.format(k="tc2_gemm", m="3xtf32"), "where": _WHERE},
+        "bytes": 4320433408 + 262098944, "sha": "8caeb4a95d22",
+        "kernel": "tc2_gemm_kernel<3xTF32> (lo parts loaded too)", "read": 4320433408,
+        "write": 262098944, "command": _NCU.format(k="tc2_gemm", m="3xtf32"), "where": _WHERE},
     ("bf16", "transformer-layer 16384x14336x4096 bf16"): {
-        "bytes": 1009379328 + 908192768, "sha": "4f1544a5bd16", "kernel": "tc2_gemm_kernel<BF16>",
-        "read": 1009379328, "write": 908192768, "command": _NCU.format(k="tc2_gemm", m="bf16"),
+        "bytes": 972379392 + 907912960, "sha": "8caeb4a95d22", "kernel": "tc2_gemm_kernel<BF16>",
+        "read": 972379392, "write": 907912960, "command": _NCU.format(k="tc2_gemm", m="bf16"),
         "where": _WHERE},
     ("e4m3", "transformer-layer 16384x14336x4096 e4m3"): {
-        "bytes": 314055936 + 888007680, "sha": "4f1544a5bd16",
+        "bytes": 315256832 + 888218880, "sha": "8caeb4a95d22",
         "kernel": "tc2_gemm_kernel<E4M3> (B stored N x K after the transpose launch)",
-        "read": 314055936, "write": 888007680, "command": _NCU.format(k="tc2_gemm", m="e4m3"),
+        "read": 315256832, "write": 888218880, "command": _NCU.format(k="tc2_gemm", m="e4m3"),
         "where": _WHERE},
     ("simt", "square-8192 fp32"): {
-        "bytes": 2853643776 + 262315776, "sha": "cb63087d890a", "kernel": "sgemm_ring_kernel",
-        "read": 2853643776, "write": 262315776, "command": _NCU.format(k="sgemm_ring", m="simt"),
+        "bytes": 2853867520 + 262399232, "sha": "cb63087d890a", "kernel": "sgemm_ring_kernel",
+        "read": 2853867520, "write": 262399232, "command": _NCU.format(k="sgemm_ring", m="simt"),
         "where": _WHERE},
 }
 
