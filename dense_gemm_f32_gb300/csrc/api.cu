@@ -203,35 +203,42 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
            const void *B, int ldb, float *C, int ldc, int num_sms, cudaStream_t stream);
 
 // 8-bit operands: the tensor cores read them K-major only, so A stored K x M
-// and B stored K x N are first transposed into scratch (A as M x K, B as
-// N x K, pitch rounded up to 16 bytes); K-major operands whose rows are not
-// 16-byte aligned are re-pitched by run_tc as usual.
+// and B stored K x N are transposed into scratch (A as M x K, B as N x K,
+// pitch rounded up to 16 bytes), and a K-major operand whose rows are not
+// 16-byte aligned is re-pitched there, both operands in one staging launch.
 int run_tc_f8(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void *A, int lda,
               const void *B, int ldb, float *C, int ldc, int num_sms, cudaStream_t stream) {
   if (!a_t && b_t)
     return run_tc(kind, false, true, M, N, K, A, lda, B, ldb, C, ldc, num_sms, stream);
-  const int64_t kp = (K + 15) / 16 * 16;  // K-major pitch of a transposed operand
-  const size_t a_bytes = a_t ? (size_t)(((int64_t)M * kp + 255) / 256 * 256) : 0;
-  const size_t b_bytes = b_t ? 0 : (size_t)(((int64_t)N * kp + 255) / 256 * 256);
+  const int64_t kp = (K + 15) / 16 * 16;  // K-major pitch of a staged operand
+  const bool a_stage = a_t || !tma_ok(A, lda, 1);
+  const bool b_stage = !b_t || !tma_ok(B, ldb, 1);
+  const size_t a_bytes = a_stage ? (size_t)(((int64_t)M * kp + 255) / 256 * 256) : 0;
+  const size_t b_bytes = b_stage ? (size_t)(((int64_t)N * kp + 255) / 256 * 256) : 0;
   void *scratch = nullptr;
   cudaError_t e = dg::scratch_alloc(&scratch, a_bytes + b_bytes, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "scratch allocation (8-bit transpose)");
+  if (e != cudaSuccess) return cuda_fail(e, "scratch allocation (8-bit staging)");
   char *s = static_cast<char *>(scratch);
   const void *Ause = A, *Buse = B;
   int lda_use = lda, ldb_use = ldb;
-  int st = DGEMM_OK;
-  if (a_t) {  // A stored K x M -> M x K
-    e = dg::launch_transpose8(A, lda, s, kp, K, M, num_sms, stream);
+  dg::StageJob jobs[2];
+  int njobs = 0;
+  if (a_stage) {  // A stored K x M -> M x K, or M x K re-pitched
+    jobs[njobs++] = a_t ? dg::StageJob{A, lda, s, kp, K, M, true}
+                        : dg::StageJob{A, lda, s, kp, M, K, false};
     Ause = s;
     lda_use = (int)kp;
   }
-  if (e == cudaSuccess && !b_t) {  // B stored K x N -> N x K
-    e = dg::launch_transpose8(B, ldb, s + a_bytes, kp, K, N, num_sms, stream);
+  if (b_stage) {  // B stored K x N -> N x K, or N x K re-pitched
+    jobs[njobs++] = b_t ? dg::StageJob{B, ldb, s + a_bytes, kp, N, K, false}
+                        : dg::StageJob{B, ldb, s + a_bytes, kp, K, N, true};
     Buse = s + a_bytes;
     ldb_use = (int)kp;
   }
+  e = dg::launch_stage(jobs, njobs, 1, num_sms, stream);
+  int st = DGEMM_OK;
   if (e != cudaSuccess)
-    st = cuda_fail(e, "8-bit transpose launch");
+    st = cuda_fail(e, "8-bit staging launch");
   else
     st = run_tc(kind, false, true, M, N, K, Ause, lda_use, Buse, ldb_use, C, ldc, num_sms, stream);
   const cudaError_t e2 = dg::scratch_free(scratch, stream);
@@ -262,19 +269,19 @@ int run_tc(dg::TcKind kind, bool a_t, bool b_t, int M, int N, int K, const void 
     e = dg::scratch_alloc(&scratch, a_bytes + b_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "scratch allocation (re-pitch)");
     char *s = static_cast<char *>(scratch);
-    dg::RepitchJob jobs[2];
+    dg::StageJob jobs[2];
     int njobs = 0;
     if (!a_ok) {
-      jobs[njobs++] = {A, lda, s, lda2, a_rows, a_cols};
+      jobs[njobs++] = {A, lda, s, lda2, a_rows, a_cols, false};
       Ause = s;
       lda_use = lda2;
     }
     if (!b_ok) {
-      jobs[njobs++] = {B, ldb, s + a_bytes, ldb2, b_rows, b_cols};
+      jobs[njobs++] = {B, ldb, s + a_bytes, ldb2, b_rows, b_cols, false};
       Buse = s + a_bytes;
       ldb_use = ldb2;
     }
-    e = dg::launch_repitch(jobs, njobs, es, num_sms, stream);  // both operands, one launch
+    e = dg::launch_stage(jobs, njobs, es, num_sms, stream);  // both operands, one launch
     if (e != cudaSuccess) goto done;
   }
   {
@@ -357,19 +364,19 @@ int run_tc_noalloc(dg::TcKind kind, int M, int N, int K, const float *A, int lda
     const int st = noalloc_scratch(dev, &base);
     if (st != DGEMM_OK) return st;
     char *s = static_cast<char *>(base);
-    dg::RepitchJob jobs[2];
+    dg::StageJob jobs[2];
     int njobs = 0;
     if (!a_ok) {
-      jobs[njobs++] = {A, lda, s, lda2, M, K};
+      jobs[njobs++] = {A, lda, s, lda2, M, K, false};
       Ause = s;
       lda_use = lda2;
     }
     if (!b_ok) {
-      jobs[njobs++] = {B, ldb, s + a_bytes, ldb2, K, N};
+      jobs[njobs++] = {B, ldb, s + a_bytes, ldb2, K, N, false};
       Buse = s + a_bytes;
       ldb_use = ldb2;
     }
-    e = dg::launch_repitch(jobs, njobs, es, num_sms, stream);
+    e = dg::launch_stage(jobs, njobs, es, num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "re-pitch launch (no-alloc)");
   }
   // 3xTF32 on the CTA-pair kernel when the lo parts fit in the rest of the

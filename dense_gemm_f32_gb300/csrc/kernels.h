@@ -62,26 +62,25 @@ DG_DECLARE_TC_UNIT(2)
 DG_DECLARE_TC_UNIT(3)
 #undef DG_DECLARE_TC_UNIT
 
-// dst = src^T for a rows x cols matrix of bytes (leading dimensions in
-// bytes): dst is cols x rows with leading dimension ldd >= rows.  Puts 8-bit
-// operands into the K-major layout (A as M x K, B as N x K).
-cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
-                              int cols, int num_sms, cudaStream_t stream);
-
-// Copy a rows x cols matrix of elem_bytes-sized elements (4, 2 or 1) from
-// (src, lds) to (dst, ldd), the padding columns up to ldd zeroed; used to
-// re-pitch operands whose rows do not start on 16-byte boundaries (dst
-// 16-byte aligned, ldd * elem_bytes a multiple of 16).  Up to two jobs (A and
-// B) go out in one launch.
-struct RepitchJob {
+// Staging of operands TMA cannot read as they are, up to two jobs (A and B)
+// in one launch.  A re-pitch copies a rows x cols matrix of elem_bytes-sized
+// elements (4, 2 or 1) from (src, lds) to (dst, ldd), the padding columns up
+// to ldd zeroed: operands whose rows do not start on 16-byte boundaries (dst
+// 16-byte aligned, ldd * elem_bytes a multiple of 16).  A transpose (8-bit
+// elements only) writes dst = src^T, cols x rows with ldd >= rows: 8-bit
+// operands into the K-major layout the tensor cores read (A as M x K, B as
+// N x K).  Leading dimensions are in elements; jobs with no rows or columns
+// are skipped.
+struct StageJob {
   const void *src;
   int64_t lds;
   void *dst;
   int64_t ldd;
-  int rows, cols;
+  int rows, cols;  // of the source
+  bool transpose;
 };
-cudaError_t launch_repitch(const RepitchJob *jobs, int njobs, int elem_bytes, int num_sms,
-                           cudaStream_t stream);
+cudaError_t launch_stage(const StageJob *jobs, int njobs, int elem_bytes, int num_sms,
+                         cudaStream_t stream);
 
 // 3xTF32 split pre-pass: A_lo = lo(A) (a_rows x a_cols, leading dimension
 // lda) and B_lo = lo(B) likewise, lo(x) = x - trunc_tf32(x) rounded to TF32

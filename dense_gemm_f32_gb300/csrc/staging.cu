@@ -7,7 +7,8 @@
 // data alignment among the conditions for the tensor cores to be used).  An
 // operand whose rows miss that (e.g. an odd leading dimension) is copied once
 // into scratch with its pitch rounded up to 16 bytes and the padding columns
-// zeroed, and the GEMM reads the copy.
+// zeroed, and the GEMM reads the copy.  Whatever a call needs for its two
+// operands (a re-pitch, a transpose, one of each) goes out in one launch.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -18,92 +19,128 @@
 namespace dg {
 namespace {
 
-// One operand of a re-pitch launch.
-struct RepitchOp {
+// One job of a staging launch, in bytes.
+struct StageOp {
   const uint8_t *src;
   uint8_t *dst;
-  int64_t lds_bytes, ldd_bytes, row_bytes;
-  int rows;
+  int64_t lds, ldd;   // leading dimensions (bytes)
+  int64_t row_bytes;  // bytes of a source row
+  int rows, cols;     // source rows; source columns (bytes)
+  int transpose;      // 1: byte transpose, 0: re-pitch
+  int aux;            // transpose: 32-bit words allowed; re-pitch: log2(threads per row)
 };
 
-__global__ void repitch_kernel(RepitchOp op0, RepitchOp op1, int es) {
-  // One 16-byte destination chunk per thread-iteration (dst rows are
-  // 16-byte aligned, ldd_bytes a multiple of 16): 16 / es element loads from
-  // the unaligned source row, one 128-bit store; columns past the row are
-  // zeroed.  Rows run along y, chunks along x, so there is no division per
-  // element; the operand is grid z (chosen field by field: indexing a
-  // parameter array with blockIdx.z would copy the parameters to local memory
-  // in every thread).
-  pdl_launch_dependents();
-  pdl_wait();
-  const bool second = blockIdx.z != 0;
-  const uint8_t *__restrict__ src = second ? op1.src : op0.src;
-  uint8_t *__restrict__ dst = second ? op1.dst : op0.dst;
-  const int64_t lds_bytes = second ? op1.lds_bytes : op0.lds_bytes;
-  const int64_t ldd_bytes = second ? op1.ldd_bytes : op0.ldd_bytes;
-  const int64_t row_bytes = second ? op1.row_bytes : op0.row_bytes;
-  const int rows = second ? op1.rows : op0.rows;
-  const int64_t chunks = ldd_bytes / 16;
-  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
-    const uint8_t *srow = src + (int64_t)r * lds_bytes;
-    uint4 *drow = reinterpret_cast<uint4 *>(dst + (int64_t)r * ldd_bytes);
-    for (int64_t ch = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; ch < chunks;
-         ch += (int64_t)gridDim.x * blockDim.x) {
-      const int64_t c0 = ch * 16;
-      uint32_t w[4];
-      if (es == 1) {
+// Bytes off .. off + 15 of the 32 bytes x then y (little-endian words).  off
+// is a multiple of the element size ES: 4-byte elements need only a choice of
+// words, narrower ones a funnel shift as well.
+template <int ES>
+__device__ __forceinline__ uint4 bytes_at(uint4 x, uint4 y, int off) {
+  const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+  const int s = off >> 2;
+  uint32_t a[5];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t v = 0;
+  for (int j = 0; j < 5; ++j) a[j] = s == 0 ? w[j] : s == 1 ? w[j + 1] : s == 2 ? w[j + 2] : w[j + 3];
+  if constexpr (ES == 4) {
+    return make_uint4(a[0], a[1], a[2], a[3]);
+  } else {
+    const int sh = 8 * (off & 3);
+    return make_uint4(__funnelshift_r(a[0], a[1], sh), __funnelshift_r(a[1], a[2], sh),
+                      __funnelshift_r(a[2], a[3], sh), __funnelshift_r(a[3], a[4], sh));
+  }
+}
+
+// Row bytes [pos, pos + 16) (pos a multiple of 16), zero past the row's end,
+// by element-sized loads of the elements inside the row, all issued before any
+// is combined.
+template <int ES>
+__device__ __forceinline__ uint4 row_chunk(const uint8_t *__restrict__ srow, int64_t pos,
+                                           int64_t row_bytes) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-          for (int b = 0; b < 4; ++b)
-            if (c0 + 4 * k + b < row_bytes) v |= (uint32_t)srow[c0 + 4 * k + b] << (8 * b);
-          w[k] = v;
-        }
-      } else if (es == 4) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          w[k] = c0 + 4 * k < row_bytes ? *reinterpret_cast<const uint32_t *>(srow + c0 + 4 * k)
-                                        : 0u;
+  for (int k = 0; k < 16; k += ES) {
+    if (pos + k < row_bytes) {
+      uint32_t e;
+      if constexpr (ES == 4)
+        e = *reinterpret_cast<const uint32_t *>(srow + pos + k);
+      else if constexpr (ES == 2)
+        e = *reinterpret_cast<const uint16_t *>(srow + pos + k);
+      else
+        e = srow[pos + k];
+      w[k >> 2] |= e << (8 * (k & 3));
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Re-pitch of ES-byte elements: destination row r is the source row's bytes
+// followed by zeros up to ldd (the destination 16-byte aligned, ldd a
+// multiple of 16).  A 16-byte destination chunk whose source bytes straddle
+// two aligned 16-byte blocks lying wholly inside the row is made from two
+// 128-bit loads; the chunks at the row's two ends load their own elements, so
+// no byte outside the row is read.  Either way a chunk costs one memory round
+// trip.  A block's 1 << aux threads share a row, so that short rows fill the
+// block with several rows instead of leaving threads idle.
+template <int ES>
+__device__ __forceinline__ void repitch_rows(const StageOp &op, int bid, int nblocks) {
+  const int lg = op.aux;
+  const int cx = 1 << lg;
+  const int lane = (int)threadIdx.x & (cx - 1);
+  const int rpb = (int)blockDim.x >> lg;  // rows per block
+  const int chunks = (int)(op.ldd / 16);
+  const int64_t row_bytes = op.row_bytes;
+  for (int64_t r = (int64_t)bid * rpb + ((int)threadIdx.x >> lg); r < op.rows;
+       r += (int64_t)nblocks * rpb) {
+    const uint8_t *srow = op.src + r * op.lds;
+    const int off = (int)(reinterpret_cast<uintptr_t>(srow) & 15);
+    // Aligned block b covers row bytes [16 b - off, 16 b - off + 16), and
+    // chunk ch (row bytes [16 ch, 16 ch + 16)) is bytes off .. off + 15 of
+    // blocks ch and ch + 1 (block ch alone if off = 0).  Those blocks lie
+    // wholly inside the row for ch in [ch_lo, ch_hi).
+    const uint4 *blocks = reinterpret_cast<const uint4 *>(srow - off);
+    const int ch_lo = off != 0;
+    const int64_t hi = (row_bytes + off - (off != 0 ? 16 : 0)) / 16;
+    const int ch_hi = hi < 0 ? 0 : hi > chunks ? chunks : (int)hi;
+    uint4 *drow = reinterpret_cast<uint4 *>(op.dst + r * op.ldd);
+    for (int ch = lane; ch < chunks; ch += cx) {
+      uint4 v;
+      if (ch >= ch_lo && ch < ch_hi) {
+        const uint4 x = __ldg(blocks + ch);
+        const uint4 y = off != 0 ? __ldg(blocks + ch + 1) : x;
+        v = bytes_at<ES>(x, y, off);
       } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t lo = c0 + 4 * k < row_bytes
-                                  ? *reinterpret_cast<const uint16_t *>(srow + c0 + 4 * k) : 0u;
-          const uint32_t hi = c0 + 4 * k + 2 < row_bytes
-                                  ? *reinterpret_cast<const uint16_t *>(srow + c0 + 4 * k + 2) : 0u;
-          w[k] = lo | (hi << 16);
-        }
+        v = row_chunk<ES>(srow, 16 * (int64_t)ch, row_bytes);
       }
-      drow[ch] = make_uint4(w[0], w[1], w[2], w[3]);
+      drow[ch] = v;
     }
   }
 }
 
-// dst = src^T for a rows x cols matrix of bytes: dst[c][r] = src[r][c].
-// 64 x 64-byte tiles, 256 threads.  Interior tiles whose rows are 4-byte
+// Byte transpose: dst[c][r] = src[r][c] for the rows x cols source, over
+// 64 x 64-byte tiles (256 threads).  Interior tiles whose rows are 4-byte
 // aligned move 32-bit words: each thread loads four words of one 4 x 4-byte
 // block through shared memory and transposes it in registers with byte
 // permutes; sixteen threads cover 64 contiguous bytes of an output row.
-// Edge tiles and unaligned operands go byte by byte.
+// Edge tiles and unaligned operands go byte by byte, each thread's sixteen
+// loads issued together (a tile then costs one memory round trip, not one
+// per byte a thread moves).
 constexpr int kT = 64;
-__global__ void __launch_bounds__(256)
-    transpose8_kernel(const uint8_t *__restrict__ src, int64_t lds, uint8_t *__restrict__ dst,
-                      int64_t ldd, int rows, int cols, int words_ok) {
-  __shared__ uint32_t tile[kT][kT / 4 + 1];
-  pdl_launch_dependents();
-  pdl_wait();
+constexpr int kTileBytes = kT * (kT / 4 + 1) * 4;  // dynamic shared memory of a transposing launch
+__device__ __forceinline__ void transpose_tiles(const StageOp &op, int bid, int nblocks,
+                                                uint32_t (*tile)[kT / 4 + 1]) {
   const int tid = threadIdx.x;
+  const int rows = op.rows, cols = op.cols;
+  const uint8_t *__restrict__ src = op.src;
+  uint8_t *__restrict__ dst = op.dst;
   const int tiles_c = (cols + kT - 1) / kT;
   const int64_t ntiles = (int64_t)((rows + kT - 1) / kT) * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  for (int64_t t = bid; t < ntiles; t += nblocks) {
     const int r0 = (int)(t / tiles_c) * kT, c0 = (int)(t % tiles_c) * kT;
-    const bool full = words_ok && r0 + kT <= rows && c0 + kT <= cols;
+    const bool full = op.aux && r0 + kT <= rows && c0 + kT <= cols;
     if (full) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int r = tid / 16 + 16 * k, w = tid % 16;
-        tile[r][w] = *reinterpret_cast<const uint32_t *>(src + (int64_t)(r0 + r) * lds + c0 + 4 * w);
+        tile[r][w] = *reinterpret_cast<const uint32_t *>(src + (int64_t)(r0 + r) * op.lds + c0 + 4 * w);
       }
       __syncthreads();
       const int cb = tid / 16, rb = tid % 16;  // 4-column block, 4-row block
@@ -115,16 +152,51 @@ __global__ void __launch_bounds__(256)
                              __byte_perm(t2, t3, 0x5410), __byte_perm(t2, t3, 0x7632)};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint32_t *>(dst + (int64_t)(c0 + 4 * cb + j) * ldd + r0 + 4 * rb) = o[j];
+        *reinterpret_cast<uint32_t *>(dst + (int64_t)(c0 + 4 * cb + j) * op.ldd + r0 + 4 * rb) = o[j];
       __syncthreads();
-    } else {
-      for (int e = tid; e < kT * kT; e += blockDim.x) {
-        const int i = e / kT, j = e % kT;  // output row c0 + i, output column r0 + j
+    } else {  // 16 bytes a thread, every load in flight before the first store
+      constexpr int kPer = kT * kT / 256;
+      uint32_t v[kPer / 4] = {};  // byte k of the thread in byte k % 4 of word k / 4
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = tid / kT + (256 / kT) * k, j = tid % kT;  // output row c0 + i, column r0 + j
         if (c0 + i < cols && r0 + j < rows)
-          dst[(int64_t)(c0 + i) * ldd + r0 + j] = src[(int64_t)(r0 + j) * lds + c0 + i];
+          v[k / 4] |= (uint32_t)src[(int64_t)(r0 + j) * op.lds + c0 + i] << (8 * (k % 4));
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = tid / kT + (256 / kT) * k, j = tid % kT;
+        if (c0 + i < cols && r0 + j < rows)
+          dst[(int64_t)(c0 + i) * op.ldd + r0 + j] = (uint8_t)(v[k / 4] >> (8 * (k % 4)));
       }
     }
   }
+}
+
+// Up to two staging jobs in one launch, of ES-byte elements (transposes for
+// ES = 1 only): blocks [0, blocks0) take job 0, the rest job 1 (the job
+// chosen field by field: indexing a parameter array by block would copy the
+// parameters to local memory in every thread).  A job's role is uniform over
+// a block, so the transpose's block barriers are safe.  Shared memory is
+// dynamic and given only to launches with a transpose, so that re-pitch
+// blocks leave room for the GEMM's CTAs, which are launched beside them
+// (programmatic dependent launch) and wait for them to finish.
+template <int ES>
+__global__ void __launch_bounds__(256, 8) stage_kernel(StageOp j0, StageOp j1, int blocks0) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const bool first = (int)blockIdx.x < blocks0;
+  const StageOp op = first ? j0 : j1;
+  const int bid = first ? (int)blockIdx.x : (int)blockIdx.x - blocks0;
+  const int nblocks = first ? blocks0 : (int)gridDim.x - blocks0;
+  if constexpr (ES == 1) {
+    if (op.transpose) {
+      extern __shared__ uint32_t stage_smem[];
+      transpose_tiles(op, bid, nblocks, reinterpret_cast<uint32_t(*)[kT / 4 + 1]>(stage_smem));
+      return;
+    }
+  }
+  repitch_rows<ES>(op, bid, nblocks);
 }
 
 // lo part of the 3xTF32 split of one operand: L[r][c] = split_lo(X[r][c])
@@ -167,48 +239,48 @@ __global__ void split_lo_kernel(SplitOperand a, SplitOperand b, int blocks_a) {
 
 }  // namespace
 
-cudaError_t launch_transpose8(const void *src, int64_t lds, void *dst, int64_t ldd, int rows,
-                              int cols, int num_sms, cudaStream_t stream) {
-  if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const int64_t ntiles = (int64_t)((rows + kT - 1) / kT) * ((cols + kT - 1) / kT);
-  int64_t grid = (int64_t)num_sms * 8;
-  if (grid > ntiles) grid = ntiles;
-  const bool words_ok = reinterpret_cast<uintptr_t>(src) % 4 == 0 && lds % 4 == 0 &&
-                        reinterpret_cast<uintptr_t>(dst) % 4 == 0 && ldd % 4 == 0;
-  const cudaError_t e = launch_kernel(transpose8_kernel, dim3((unsigned)grid), dim3(256), 0, stream, 1,
-                                      static_cast<const uint8_t *>(src), lds,
-                                      static_cast<uint8_t *>(dst), ldd, rows, cols,
-                                      words_ok ? 1 : 0);
-  if (e == cudaSuccess) count_launch();
-  return e;
-}
-
-cudaError_t launch_repitch(const RepitchJob *jobs, int njobs, int elem_bytes, int num_sms,
-                           cudaStream_t stream) {
-  RepitchOp ops[2] = {};
-  int n = 0, max_rows = 0;
-  int64_t max_chunks = 0;
-  for (int j = 0; j < njobs && j < 2; ++j) {
-    if (jobs[j].rows <= 0) continue;
-    RepitchOp &o = ops[n++];
-    o.src = static_cast<const uint8_t *>(jobs[j].src);
-    o.dst = static_cast<uint8_t *>(jobs[j].dst);
-    o.lds_bytes = jobs[j].lds * elem_bytes;
-    o.ldd_bytes = jobs[j].ldd * elem_bytes;
-    o.row_bytes = (int64_t)jobs[j].cols * elem_bytes;
-    o.rows = jobs[j].rows;
-    const int64_t chunks = o.ldd_bytes / 16;
-    max_chunks = chunks > max_chunks ? chunks : max_chunks;
-    max_rows = o.rows > max_rows ? o.rows : max_rows;
+cudaError_t launch_stage(const StageJob *jobs, int njobs, int elem_bytes, int num_sms,
+                         cudaStream_t stream) {
+  StageOp ops[2] = {};
+  int blocks[2] = {0, 0};
+  int n = 0;
+  for (int j = 0; j < njobs && j < 2; ++j)
+    if (jobs[j].rows > 0 && jobs[j].cols > 0) ++n;
+  for (int j = 0, k = 0; j < njobs && j < 2; ++j) {
+    const StageJob &jb = jobs[j];
+    if (jb.rows <= 0 || jb.cols <= 0) continue;
+    StageOp &o = ops[k];
+    o.src = static_cast<const uint8_t *>(jb.src);
+    o.dst = static_cast<uint8_t *>(jb.dst);
+    o.lds = jb.lds * elem_bytes;
+    o.ldd = jb.ldd * elem_bytes;
+    o.row_bytes = (int64_t)jb.cols * elem_bytes;
+    o.rows = jb.rows;
+    o.cols = jb.cols * elem_bytes;
+    o.transpose = jb.transpose ? 1 : 0;
+    int64_t b;
+    if (jb.transpose) {  // 64 x 64 tiles, up to 8 blocks per SM
+      o.aux = reinterpret_cast<uintptr_t>(jb.src) % 4 == 0 && o.lds % 4 == 0 &&
+              reinterpret_cast<uintptr_t>(jb.dst) % 4 == 0 && o.ldd % 4 == 0;
+      b = (int64_t)((o.rows + kT - 1) / kT) * ((o.cols + kT - 1) / kT);
+      if (b > (int64_t)num_sms * 8) b = (int64_t)num_sms * 8;
+    } else {  // threads per row: the chunks of a row rounded up to a power of two, at most 256
+      const int64_t chunks = o.ldd / 16;
+      int lg = 0;
+      while (lg < 8 && ((int64_t)1 << lg) < chunks) ++lg;
+      o.aux = lg;
+      const int rpb = 256 >> lg;
+      b = (o.rows + rpb - 1) / rpb;
+      if (b > (int64_t)num_sms * 16 / n) b = (int64_t)num_sms * 16 / n;
+    }
+    blocks[k++] = (int)(b < 1 ? 1 : b);
   }
   if (n == 0) return cudaSuccess;
-  const int bx = (int)((max_chunks + 255) / 256 < 8 ? (max_chunks + 255) / 256 : 8);
-  int64_t by = (int64_t)num_sms * 16 / (bx * n);
-  if (by > max_rows) by = max_rows;
-  if (by > 65535) by = 65535;
-  if (by < 1) by = 1;
-  const cudaError_t e = launch_kernel(repitch_kernel, dim3((unsigned)bx, (unsigned)by, (unsigned)n),
-                                      dim3(256), 0, stream, 1, ops[0], ops[1], elem_bytes);
+  const size_t smem = ops[0].transpose || ops[1].transpose ? kTileBytes : 0;
+  void (*kern)(StageOp, StageOp, int) =
+      elem_bytes == 4 ? stage_kernel<4> : elem_bytes == 2 ? stage_kernel<2> : stage_kernel<1>;
+  const cudaError_t e = launch_kernel(kern, dim3((unsigned)(blocks[0] + blocks[1])), dim3(256), smem,
+                                      stream, 1, ops[0], ops[1], blocks[0]);
   if (e == cudaSuccess) count_launch();
   return e;
 }
