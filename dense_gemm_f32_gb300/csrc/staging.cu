@@ -244,8 +244,10 @@ cudaError_t launch_stage(const StageJob *jobs, int njobs, int elem_bytes, int nu
   StageOp ops[2] = {};
   int blocks[2] = {0, 0};
   int n = 0;
-  for (int j = 0; j < njobs && j < 2; ++j)
+  for (int j = 0; j < njobs && j < 2; ++j) {
+    if (jobs[j].transpose && elem_bytes != 1) return cudaErrorInvalidValue;  // 8-bit only
     if (jobs[j].rows > 0 && jobs[j].cols > 0) ++n;
+  }
   for (int j = 0, k = 0; j < njobs && j < 2; ++j) {
     const StageJob &jb = jobs[j];
     if (jb.rows <= 0 || jb.cols <= 0) continue;
